@@ -1,0 +1,204 @@
+"""CPU oracle for block-sparse causal document-local GQA - TEST INFRASTRUCTURE.
+
+A plain fp64 C/OpenMP statement of what MSA computes (see msa_oracle.c for the
+definitions and the pages they follow), loaded with ctypes.  Only the tests,
+``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may use this
+package; the product (``block_sparse_gqa_msa_gb300``) never imports it and
+shares no code with it.
+
+Inputs are CPU torch tensors (bf16 tensors are widened exactly to fp64 here),
+uint16 numpy arrays holding bf16 bit patterns, or float64 numpy arrays (used
+unrounded, e.g. by finite-difference tests).  Outputs are float64 arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libmsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OR_OK, OR_BAD_ARGS, OR_BAD_Q2K, OR_CAPACITY = 0, 1, 2, 3
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False, extra_flags: tuple[str, ...] = (), out: str | None = None) -> str:
+    """Compile msa_oracle.c with gcc (-O2, OpenMP).  Returns the .so path."""
+    out = out or _LIB_PATH
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC) and not extra_flags):
+        return out
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c99", *extra_flags,
+           "-o", out, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _load(path: str | None = None):
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_D = ctypes.c_double
+
+
+def _bind(lib):
+    lib.oracle_forward.argtypes = [_P, _P, _P, _P, _I64, _P, _I32, _D, _P, _I64, _P, _P]
+    lib.oracle_dq.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _I32, _D, _P, _I64, _P, _P]
+    lib.oracle_dkv_blocks.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _I32, _D, _P, _I64, _P, _P]
+    lib.oracle_backward.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _I32, _D, _P, _P, _P]
+    lib.oracle_plan.argtypes = [_P, _I64, _P, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _I64, _P]
+    lib.oracle_pair_count.argtypes = [_P, _I64, _P, _I32]
+    lib.oracle_pair_count.restype = _I64
+    for f in ("oracle_forward", "oracle_dq", "oracle_dkv_blocks", "oracle_backward",
+              "oracle_plan"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact fp64 copy of a bf16 tensor / uint16 bf16 bit array / fp64 array."""
+    if isinstance(x, np.ndarray):
+        if x.dtype == np.uint16:
+            return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        if x.dtype == np.float64:
+            return np.ascontiguousarray(x)
+        raise TypeError("expected uint16 bf16 bit patterns or float64")
+    import torch
+    if x.dtype not in (torch.bfloat16, torch.float64):
+        raise TypeError("expected a bfloat16 or float64 tensor")
+    return np.ascontiguousarray(x.detach().cpu().to(torch.float64).numpy())
+
+
+def _i32(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != OR_OK:
+        raise OracleError(f"{what}: oracle returned {rc}")
+
+
+class Problem:
+    """Holds the converted inputs of one MSA problem for repeated oracle calls."""
+
+    def __init__(self, q, k, v, q2k, doc_offsets, scale, do=None, lib_path: str | None = None):
+        self.q = _f64(q)
+        self.k = _f64(k)
+        self.v = _f64(v)
+        self.do = None if do is None else _f64(do)
+        self.q2k = _i32(q2k)
+        self.offs = _i32(doc_offsets)
+        self.T = int(self.q.shape[0])
+        self.D = int(self.offs.size - 1)
+        self.scale = float(scale)
+        self.lib = _load(lib_path)
+
+    @classmethod
+    def from_workload(cls, w, lib_path: str | None = None):
+        return cls(w.q, w.k, w.v, w.q2k, w.doc_offsets, w.scale, do=w.do, lib_path=lib_path)
+
+    def forward(self, toks=None):
+        """(O [n,64,128], LSE [n,64]) for the listed tokens (all if None)."""
+        tk = None if toks is None else np.ascontiguousarray(toks, dtype=np.int64)
+        n = self.T if tk is None else tk.size
+        O = np.zeros((n, 64, 128), dtype=np.float64)
+        L = np.zeros((n, 64), dtype=np.float64)
+        rc = self.lib.oracle_forward(_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.q2k),
+                                     self.T, _ptr(self.offs), self.D, self.scale, _ptr(tk), n,
+                                     _ptr(O), _ptr(L))
+        _check(rc, "forward")
+        return O, L
+
+    def dq(self, toks=None, with_delta: bool = False):
+        tk = None if toks is None else np.ascontiguousarray(toks, dtype=np.int64)
+        n = self.T if tk is None else tk.size
+        dQ = np.zeros((n, 64, 128), dtype=np.float64)
+        delta = np.zeros((n, 64), dtype=np.float64) if with_delta else None
+        rc = self.lib.oracle_dq(_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.do),
+                                _ptr(self.q2k), self.T, _ptr(self.offs), self.D, self.scale,
+                                _ptr(tk), n, _ptr(dQ), _ptr(delta))
+        _check(rc, "dq")
+        return (dQ, delta) if with_delta else dQ
+
+    def dkv_blocks(self, blocks):
+        """blocks: list of (g, first key token of a 128-key document block)."""
+        b = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64).reshape(-1, 2))
+        n = b.shape[0]
+        dK = np.zeros((n, 128, 128), dtype=np.float64)
+        dV = np.zeros((n, 128, 128), dtype=np.float64)
+        rc = self.lib.oracle_dkv_blocks(_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.do),
+                                        _ptr(self.q2k), self.T, _ptr(self.offs), self.D,
+                                        self.scale, _ptr(b), n, _ptr(dK), _ptr(dV))
+        _check(rc, "dkv_blocks")
+        return dK, dV
+
+    def backward(self):
+        """(dQ [T,64,128], dK [T,4,128], dV [T,4,128]) in full."""
+        dQ = np.zeros((self.T, 64, 128), dtype=np.float64)
+        dK = np.zeros((self.T, 4, 128), dtype=np.float64)
+        dV = np.zeros((self.T, 4, 128), dtype=np.float64)
+        rc = self.lib.oracle_backward(_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.do),
+                                      _ptr(self.q2k), self.T, _ptr(self.offs), self.D,
+                                      self.scale, _ptr(dQ), _ptr(dK), _ptr(dV))
+        _check(rc, "backward")
+        return dQ, dK, dV
+
+    def pair_count(self) -> int:
+        n = self.lib.oracle_pair_count(_ptr(self.q2k), self.T, _ptr(self.offs), self.D)
+        if n < 0:
+            raise OracleError("pair_count: invalid input")
+        return int(n)
+
+    def plan(self, super_block: int = 16):
+        """Canonical k2q CSR and task table (see oracle_plan in msa_oracle.c)."""
+        return plan(self.q2k, self.offs, self.T, super_block, lib=self.lib)
+
+
+def plan(q2k, doc_offsets, T: int, super_block: int = 16, lib=None):
+    lib = lib or _load()
+    q2k = _i32(q2k)
+    offs = _i32(doc_offsets)
+    D = offs.size - 1
+    nb_cap = (T + 127) // 128 + D
+    row_ptr = np.zeros(4 * nb_cap + 1, dtype=np.int64)
+    col = np.zeros(64 * T, dtype=np.int32)
+    task_cap = 8 * T + 4 * nb_cap * (nb_cap + 1) // 2 + 16
+    tasks = np.zeros((task_cap, 3), dtype=np.int64)
+    nblk = np.zeros(D, dtype=np.int32)
+    blk_base = np.zeros(D, dtype=np.int32)
+    counts = np.zeros(3, dtype=np.int64)
+    rc = lib.oracle_plan(_ptr(q2k), T, _ptr(offs), D, super_block, _ptr(nblk), _ptr(blk_base),
+                         _ptr(row_ptr), row_ptr.size, _ptr(col), col.size, _ptr(tasks), task_cap,
+                         _ptr(counts))
+    _check(rc, "plan")
+    NB, nnz, nt = (int(x) for x in counts)
+    return {
+        "NB": NB, "nnz": nnz, "ntasks": nt, "nblk": nblk, "blk_base": blk_base,
+        "row_ptr": row_ptr[: 4 * NB + 1].copy(), "col": col[:nnz].copy(),
+        "tasks": tasks[:nt].copy(),
+    }

@@ -1,0 +1,491 @@
+/*
+ * msa_oracle.c - TEST INFRASTRUCTURE ONLY.  A plain, slow, fp64 CPU statement
+ * of block-sparse, causal, document-local grouped-query attention (MiniMax
+ * Sparse Attention, "MSA") and of the k2q plan derived from its selection.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this library; the product path never does.  It shares no code with
+ * the CUDA path.
+ *
+ * Sources (web pages on the method):
+ *   [PR]  NeMo-Automodel PR "feat(minimax-m3): add SM100 MSA sparse attention
+ *         with custom backward" - sections "Changelog" (compact document-local
+ *         q2k indices), "Design" (the flat-attention interface
+ *         Q[T,64,128], K/V[T,4,128], int32 q2k[4,T,16], -1 for unused slots,
+ *         layout = document offsets) and "Supported scope" (64 query / 4 KV /
+ *         4 index heads, head dim 128, block 128, top-k 16, causal prefill).
+ *   [BWD] API page "msa_backward_sm100" - module description (task rows of
+ *         8 queries x 16 main heads bucketed by (index_head, key_block);
+ *         delta preprocess), run_backward parameter list (LSE is FP32 [T,64]).
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - query head h uses KV head and index head h/16;
+ *   - key block v of a document covers document positions 128v..128v+127 (the
+ *     last block may be partial);
+ *   - the slots of q2k[g,t,:] form a SET (duplicates count once);
+ *   - a selected block after the query's own block contributes no keys;
+ *   - a value < -1 or >= the document's block count is an error;
+ *   - LSE is the natural-log log-sum-exp of the scaled scores;
+ *   - a row with no visible key has O = 0, LSE = -inf and zero gradients;
+ *   - delta = rowsum(dO * O) is taken from the oracle's own exact O.
+ *
+ * Inputs: fp64 arrays.  The Python wrapper widens the bf16 tensors of a
+ * problem exactly (bf16 -> fp32 -> fp64), so the oracle sees the same values
+ * the GPU path reads; finite-difference tests pass unrounded fp64 values.
+ * All arithmetic is fp64.  Parallelism is OpenMP over independent
+ * rows / buckets only; there is no blocking or fusion beyond the definitions.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define NQH 64   /* query heads */
+#define NKV 4    /* KV heads = index heads */
+#define HPG 16   /* query heads per index head */
+#define HD 128   /* head dim */
+#define BLK 128  /* key block size */
+#define TOPK 16  /* q2k slots */
+
+enum { OR_OK = 0, OR_BAD_ARGS = 1, OR_BAD_Q2K = 2, OR_CAPACITY = 3 };
+
+/* Document offsets: offs[0] = 0, strictly increasing, offs[D] = T. */
+static int check_offsets(const int32_t* offs, int32_t D, int64_t T) {
+  if (D <= 0 || offs[0] != 0 || offs[D] != T) return OR_BAD_ARGS;
+  for (int32_t d = 0; d < D; ++d)
+    if (offs[d + 1] <= offs[d]) return OR_BAD_ARGS;
+  return OR_OK;
+}
+
+static int32_t doc_of(const int32_t* offs, int32_t D, int64_t t) {
+  int32_t lo = 0, hi = D - 1; /* largest d with offs[d] <= t */
+  while (lo < hi) {
+    int32_t mid = (lo + hi + 1) / 2;
+    if (offs[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+static int32_t nblocks(int32_t len) { return (len + BLK - 1) / BLK; }
+
+/* Sel(t,g) as a membership array over the document's blocks; returns
+ * OR_BAD_Q2K if a slot holds a value outside [-1, nblk). */
+static int selection(const int32_t* q2k, int64_t T, int g, int64_t t, int32_t nblk,
+                     unsigned char* sel) {
+  memset(sel, 0, (size_t)nblk);
+  for (int i = 0; i < TOPK; ++i) {
+    int32_t v = q2k[((int64_t)g * T + t) * TOPK + i];
+    if (v == -1) continue;
+    if (v < -1 || v >= nblk) return OR_BAD_Q2K;
+    sel[v] = 1;
+  }
+  return OR_OK;
+}
+
+/* Keys(t,g) = { s_d + j : 0 <= j <= p, floor(j/128) in Sel(t,g) }, ascending. */
+static int keys_of(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, int g,
+                   int64_t t, int64_t* keys, int64_t* nkeys, unsigned char* sel) {
+  int32_t d = doc_of(offs, D, t);
+  int64_t s = offs[d];
+  int32_t len = offs[d + 1] - offs[d];
+  int64_t p = t - s;
+  int rc = selection(q2k, T, g, t, nblocks(len), sel);
+  if (rc) return rc;
+  int64_t n = 0;
+  for (int64_t j = 0; j <= p; ++j)
+    if (sel[j / BLK]) keys[n++] = s + j;
+  *nkeys = n;
+  return OR_OK;
+}
+
+/* Validate q2k in full (every slot of every token and index head). */
+static int check_q2k(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D) {
+  for (int64_t t = 0; t < T; ++t) {
+    int32_t d = doc_of(offs, D, t);
+    int32_t nb = nblocks(offs[d + 1] - offs[d]);
+    for (int g = 0; g < NKV; ++g)
+      for (int i = 0; i < TOPK; ++i) {
+        int32_t v = q2k[((int64_t)g * T + t) * TOPK + i];
+        if (v < -1 || v >= nb) return OR_BAD_Q2K;
+      }
+  }
+  return OR_OK;
+}
+
+/* scale * <Q[t,h,:], K[j,g,:]> */
+static double score(const double* Q, const double* K, int64_t t, int h, int64_t j, int g,
+                    double scale) {
+  const double* q = Q + ((int64_t)t * NQH + h) * HD;
+  const double* k = K + ((int64_t)j * NKV + g) * HD;
+  double acc = 0.0;
+  for (int c = 0; c < HD; ++c) acc += q[c] * k[c];
+  return scale * acc;
+}
+
+/* Forward of one query token t for the 16 heads of index head g:
+ * LSE[h] = ln sum_j exp(s_j), P_j = exp(s_j - LSE), O[h] = sum_j P_j V[j,g].
+ * o: [16][128], lse: [16].  s: scratch of nkeys doubles. */
+static void row_forward(const double* Q, const double* K, const double* V, int64_t t, int g,
+                        const int64_t* keys, int64_t nkeys, double scale, double* s, double* o,
+                        double* lse) {
+  for (int hh = 0; hh < HPG; ++hh) {
+    int h = g * HPG + hh;
+    double* oh = o + (int64_t)hh * HD;
+    for (int c = 0; c < HD; ++c) oh[c] = 0.0;
+    if (nkeys == 0) {
+      lse[hh] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int64_t i = 0; i < nkeys; ++i) {
+      s[i] = score(Q, K, t, h, keys[i], g, scale);
+      if (s[i] > m) m = s[i];
+    }
+    double sum = 0.0;
+    for (int64_t i = 0; i < nkeys; ++i) sum += exp(s[i] - m);
+    double L = m + log(sum);
+    lse[hh] = L;
+    for (int64_t i = 0; i < nkeys; ++i) {
+      double pr = exp(s[i] - L);
+      const double* vr = V + ((int64_t)keys[i] * NKV + g) * HD;
+      for (int c = 0; c < HD; ++c) oh[c] += pr * vr[c];
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------
+ * Forward on a list of query tokens (all 64 heads each).
+ * toks == NULL means every token 0..T-1 (ntoks must equal T).
+ * O: [ntoks][64][128], LSE: [ntoks][64].
+ */
+int oracle_forward(const double* Q, const double* K, const double* V, const int32_t* q2k,
+                   int64_t T, const int32_t* offs, int32_t D, double scale, const int64_t* toks,
+                   int64_t ntoks, double* O, double* LSE) {
+  if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
+  int64_t maxlen = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (offs[d + 1] - offs[d] > maxlen) maxlen = offs[d + 1] - offs[d];
+  int err = 0;
+#pragma omp parallel
+  {
+    int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)maxlen);
+    double* s = (double*)malloc(sizeof(double) * (size_t)maxlen);
+    unsigned char* sel = (unsigned char*)malloc((size_t)nblocks((int32_t)maxlen));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t i = 0; i < ntoks; ++i) {
+      int64_t t = toks ? toks[i] : i;
+      for (int g = 0; g < NKV; ++g) {
+        int64_t nk;
+        if (keys_of(q2k, T, offs, D, g, t, keys, &nk, sel)) {
+          err = OR_BAD_Q2K;
+          continue;
+        }
+        row_forward(Q, K, V, t, g, keys, nk, scale, s, O + (i * NQH + g * HPG) * HD,
+                    LSE + i * NQH + g * HPG);
+      }
+    }
+    free(keys);
+    free(s);
+    free(sel);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------
+ * dQ on a list of query tokens.  For L = sum(O * dO):
+ *   delta = sum_c dO * O,  dP_j = <dO, V_j>,  dS_j = P_j (dP_j - delta),
+ *   dQ = scale * sum_j dS_j K_j.
+ * O, LSE and delta are recomputed exactly here.  dQ: [ntoks][64][128].
+ * If DELTA is not NULL it receives delta [ntoks][64].
+ */
+int oracle_dq(const double* Q, const double* K, const double* V, const double* dO,
+              const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, double scale,
+              const int64_t* toks, int64_t ntoks, double* dQ, double* DELTA) {
+  if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
+  int64_t maxlen = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (offs[d + 1] - offs[d] > maxlen) maxlen = offs[d + 1] - offs[d];
+#pragma omp parallel
+  {
+    int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)maxlen);
+    double* s = (double*)malloc(sizeof(double) * (size_t)maxlen);
+    unsigned char* sel = (unsigned char*)malloc((size_t)nblocks((int32_t)maxlen));
+    double o[HPG * HD], lse[HPG];
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t i = 0; i < ntoks; ++i) {
+      int64_t t = toks ? toks[i] : i;
+      for (int g = 0; g < NKV; ++g) {
+        int64_t nk;
+        keys_of(q2k, T, offs, D, g, t, keys, &nk, sel);
+        row_forward(Q, K, V, t, g, keys, nk, scale, s, o, lse);
+        for (int hh = 0; hh < HPG; ++hh) {
+          int h = g * HPG + hh;
+          const double* dor = dO + ((int64_t)t * NQH + h) * HD;
+          double* dq = dQ + (i * NQH + h) * HD;
+          double delta = 0.0;
+          for (int c = 0; c < HD; ++c) delta += dor[c] * o[hh * HD + c];
+          if (DELTA) DELTA[i * NQH + h] = delta;
+          for (int c = 0; c < HD; ++c) dq[c] = 0.0;
+          for (int64_t kk = 0; kk < nk; ++kk) {
+            int64_t j = keys[kk];
+            double pr = exp(score(Q, K, t, h, j, g, scale) - lse[hh]);
+            const double* vr = V + (j * NKV + g) * HD;
+            const double* kr = K + (j * NKV + g) * HD;
+            double dp = 0.0;
+            for (int c = 0; c < HD; ++c) dp += dor[c] * vr[c];
+            double ds = pr * (dp - delta);
+            for (int c = 0; c < HD; ++c) dq[c] += scale * ds * kr[c];
+          }
+        }
+      }
+    }
+    free(keys);
+    free(s);
+    free(sel);
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * dK and dV of whole key blocks.  blocks: nblk_req pairs (g, global token
+ * index of the block's first key).  For each such block, every query t of the
+ * same document that sees a key of the block contributes, over its 16 heads:
+ *   dV_j += P_tj dO_t,   dK_j += scale * dS_tj Q_t.
+ * dK, dV: [nblk_req][128][128] (rows past the document end stay zero).
+ */
+int oracle_dkv_blocks(const double* Q, const double* K, const double* V,
+                      const double* dO, const int32_t* q2k, int64_t T, const int32_t* offs,
+                      int32_t D, double scale, const int64_t* blocks, int64_t nblk_req,
+                      double* dK, double* dV) {
+  if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
+  int64_t maxlen = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (offs[d + 1] - offs[d] > maxlen) maxlen = offs[d + 1] - offs[d];
+  for (int64_t b = 0; b < nblk_req; ++b) {
+    int g = (int)blocks[2 * b];
+    int64_t k0 = blocks[2 * b + 1];
+    int32_t d = doc_of(offs, D, k0);
+    int64_t s0 = offs[d], e0 = offs[d + 1];
+    if ((k0 - s0) % BLK) return OR_BAD_ARGS;
+    int64_t v = (k0 - s0) / BLK;
+    int64_t klen = (e0 - k0 < BLK) ? (e0 - k0) : BLK;
+    double* dk = dK + b * BLK * HD;
+    double* dv = dV + b * BLK * HD;
+    memset(dk, 0, sizeof(double) * BLK * HD);
+    memset(dv, 0, sizeof(double) * BLK * HD);
+    int nthr = 1;
+#ifdef _OPENMP
+    nthr = omp_get_max_threads();
+#endif
+    double* part = (double*)calloc((size_t)nthr * 2 * BLK * HD, sizeof(double));
+#pragma omp parallel
+    {
+      int tid = 0;
+#ifdef _OPENMP
+      tid = omp_get_thread_num();
+#endif
+      double* pk = part + (size_t)tid * 2 * BLK * HD;
+      double* pv = pk + BLK * HD;
+      int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)maxlen);
+      double* s = (double*)malloc(sizeof(double) * (size_t)maxlen);
+      unsigned char* sel = (unsigned char*)malloc((size_t)nblocks((int32_t)maxlen));
+      double o[HPG * HD], lse[HPG];
+#pragma omp for schedule(static)
+      for (int64_t t = k0; t < e0; ++t) {
+        selection(q2k, T, g, t, nblocks((int32_t)(e0 - s0)), sel);
+        if (!sel[v]) continue;
+        int64_t nk;
+        keys_of(q2k, T, offs, D, g, t, keys, &nk, sel);
+        row_forward(Q, K, V, t, g, keys, nk, scale, s, o, lse);
+        for (int hh = 0; hh < HPG; ++hh) {
+          int h = g * HPG + hh;
+          const double* dor = dO + (t * NQH + h) * HD;
+          const double* qr = Q + (t * NQH + h) * HD;
+          double delta = 0.0;
+          for (int c = 0; c < HD; ++c) delta += dor[c] * o[hh * HD + c];
+          for (int64_t r = 0; r < klen && k0 + r <= t; ++r) {
+            int64_t j = k0 + r;
+            double pr = exp(score(Q, K, t, h, j, g, scale) - lse[hh]);
+            const double* vr = V + (j * NKV + g) * HD;
+            double dp = 0.0;
+            for (int c = 0; c < HD; ++c) dp += dor[c] * vr[c];
+            double ds = pr * (dp - delta);
+            for (int c = 0; c < HD; ++c) {
+              pv[r * HD + c] += pr * dor[c];
+              pk[r * HD + c] += scale * ds * qr[c];
+            }
+          }
+        }
+      }
+      free(keys);
+      free(s);
+      free(sel);
+    }
+    for (int th = 0; th < nthr; ++th) {
+      const double* pk = part + (size_t)th * 2 * BLK * HD;
+      for (int64_t x = 0; x < BLK * HD; ++x) {
+        dk[x] += pk[x];
+        dv[x] += pk[BLK * HD + x];
+      }
+    }
+    free(part);
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Full backward: dQ [T][64][128], dK, dV [T][4][128].  dQ comes from
+ * oracle_dq over all tokens; dK/dV from oracle_dkv_blocks over every (index
+ * head, key block) of every document, scattered back to token rows.
+ */
+int oracle_backward(const double* Q, const double* K, const double* V, const double* dO,
+                    const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, double scale,
+                    double* dQ, double* dK, double* dV) {
+  int rc = oracle_dq(Q, K, V, dO, q2k, T, offs, D, scale, NULL, T, dQ, NULL);
+  if (rc) return rc;
+  memset(dK, 0, sizeof(double) * (size_t)T * NKV * HD);
+  memset(dV, 0, sizeof(double) * (size_t)T * NKV * HD);
+  double* bk = (double*)malloc(sizeof(double) * BLK * HD);
+  double* bv = (double*)malloc(sizeof(double) * BLK * HD);
+  for (int32_t d = 0; d < D; ++d) {
+    for (int64_t k0 = offs[d]; k0 < offs[d + 1]; k0 += BLK) {
+      int64_t klen = offs[d + 1] - k0 < BLK ? offs[d + 1] - k0 : BLK;
+      for (int g = 0; g < NKV; ++g) {
+        int64_t req[2] = {g, k0};
+        rc = oracle_dkv_blocks(Q, K, V, dO, q2k, T, offs, D, scale, req, 1, bk, bv);
+        if (rc) break;
+        for (int64_t r = 0; r < klen; ++r)
+          for (int c = 0; c < HD; ++c) {
+            dK[((k0 + r) * NKV + g) * HD + c] = bk[r * HD + c];
+            dV[((k0 + r) * NKV + g) * HD + c] = bv[r * HD + c];
+          }
+      }
+    }
+  }
+  free(bk);
+  free(bv);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------
+ * The k2q plan in canonical form.
+ *   nblk[d] = ceil(len_d / 128); blk_base[d] = sum_{d'<d} nblk[d'];
+ *   NB = sum nblk; bucket(g, d, v) = g*NB + blk_base[d] + v.
+ *   The bucket holds every query t of document d with v in Sel(t,g) and
+ *   v <= (t - s_d)/128, ascending in t (row_ptr / col CSR, 4*NB buckets).
+ *   Tasks: the bucket's queries are cut at super-block boundaries - runs of
+ *   Z consecutive query blocks (Z = 0: the whole document) - and each run is
+ *   split, in order, into chunks of at most 8 queries.  A task is
+ *   (bucket, col index of its first query, query count).
+ * Output arrays are caller-allocated; the capacities guard them.
+ * counts[0] = NB, counts[1] = nnz, counts[2] = ntasks.
+ */
+int oracle_plan(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, int32_t Z,
+                int32_t* nblk, int32_t* blk_base, int64_t* row_ptr, int64_t row_ptr_cap,
+                int32_t* col, int64_t col_cap, int64_t* tasks, int64_t task_cap,
+                int64_t* counts) {
+  if (T <= 0 || Z < 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
+  int64_t NB = 0;
+  int32_t maxnb = 0;
+  for (int32_t d = 0; d < D; ++d) {
+    nblk[d] = nblocks(offs[d + 1] - offs[d]);
+    blk_base[d] = (int32_t)NB;
+    NB += nblk[d];
+    if (nblk[d] > maxnb) maxnb = nblk[d];
+  }
+  if (4 * NB + 1 > row_ptr_cap) return OR_CAPACITY;
+  unsigned char* sel = (unsigned char*)malloc((size_t)maxnb);
+  /* count */
+  for (int64_t b = 0; b <= 4 * NB; ++b) row_ptr[b] = 0;
+  for (int g = 0; g < NKV; ++g)
+    for (int64_t t = 0; t < T; ++t) {
+      int32_t d = doc_of(offs, D, t);
+      int64_t qb = (t - offs[d]) / BLK;
+      selection(q2k, T, g, t, nblk[d], sel);
+      for (int64_t v = 0; v <= qb; ++v)
+        if (sel[v]) row_ptr[g * NB + blk_base[d] + v + 1] += 1;
+    }
+  for (int64_t b = 0; b < 4 * NB; ++b) row_ptr[b + 1] += row_ptr[b];
+  int64_t nnz = row_ptr[4 * NB];
+  if (nnz > col_cap) {
+    free(sel);
+    return OR_CAPACITY;
+  }
+  /* fill, ascending t within each bucket */
+  int64_t* fillpos = (int64_t*)malloc(sizeof(int64_t) * (size_t)(4 * NB));
+  for (int64_t b = 0; b < 4 * NB; ++b) fillpos[b] = row_ptr[b];
+  for (int g = 0; g < NKV; ++g)
+    for (int64_t t = 0; t < T; ++t) {
+      int32_t d = doc_of(offs, D, t);
+      int64_t qb = (t - offs[d]) / BLK;
+      selection(q2k, T, g, t, nblk[d], sel);
+      for (int64_t v = 0; v <= qb; ++v)
+        if (sel[v]) col[fillpos[g * NB + blk_base[d] + v]++] = (int32_t)t;
+    }
+  /* tasks */
+  int64_t nt = 0;
+  int rc = OR_OK;
+  for (int g = 0; g < NKV && !rc; ++g)
+    for (int32_t d = 0; d < D && !rc; ++d)
+      for (int32_t v = 0; v < nblk[d] && !rc; ++v) {
+        int64_t b = g * NB + blk_base[d] + v;
+        int64_t i = row_ptr[b];
+        while (i < row_ptr[b + 1]) {
+          int64_t run_sb = Z ? ((col[i] - offs[d]) / BLK) / Z : 0;
+          int64_t n = 0;
+          while (i + n < row_ptr[b + 1] && n < 8 &&
+                 (Z ? ((col[i + n] - offs[d]) / BLK) / Z : 0) == run_sb)
+            ++n;
+          if (nt >= task_cap) {
+            rc = OR_CAPACITY;
+            break;
+          }
+          tasks[3 * nt + 0] = b;
+          tasks[3 * nt + 1] = i;
+          tasks[3 * nt + 2] = n;
+          ++nt;
+          i += n;
+        }
+      }
+  counts[0] = NB;
+  counts[1] = nnz;
+  counts[2] = nt;
+  free(fillpos);
+  free(sel);
+  return rc;
+}
+
+/* Number of attended (query, head, key) triples: sum over t, g of
+ * 16 * |Keys(t,g)|.  This is the pair count the FLOP metric uses. */
+int64_t oracle_pair_count(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D) {
+  if (T <= 0 || check_offsets(offs, D, T) || check_q2k(q2k, T, offs, D)) return -1;
+  int32_t maxnb = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (nblocks(offs[d + 1] - offs[d]) > maxnb) maxnb = nblocks(offs[d + 1] - offs[d]);
+  int64_t total = 0;
+#pragma omp parallel reduction(+ : total)
+  {
+    unsigned char* sel = (unsigned char*)malloc((size_t)maxnb);
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+      int32_t d = doc_of(offs, D, t);
+      int64_t p = t - offs[d];
+      for (int g = 0; g < NKV; ++g) {
+        selection(q2k, T, g, t, nblocks(offs[d + 1] - offs[d]), sel);
+        for (int64_t v = 0; v * BLK <= p; ++v)
+          if (sel[v]) {
+            int64_t hi = (v + 1) * BLK - 1 < p ? (v + 1) * BLK - 1 : p;
+            total += HPG * (hi - v * BLK + 1);
+          }
+      }
+    }
+    free(sel);
+  }
+  return total;
+}
