@@ -1,0 +1,134 @@
+// common.cuh - shapes, plan layout and status bits shared by the MSA kernels.
+//
+// Fixed topology of the method (NeMo-Automodel PR "feat(minimax-m3): add SM100
+// MSA sparse attention with custom backward", section "Supported scope"):
+// 64 query heads, 4 KV heads, 4 index heads, head dim 128, key block 128,
+// top-16 selection.  Query head h reads KV / index head h / 16.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kQHeads = 64;
+constexpr int kKVHeads = 4;
+constexpr int kHeadsPerGroup = 16;  // query heads per index head
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 128;         // keys per block
+constexpr int kTopK = 16;           // q2k slots
+constexpr int kTaskQueries = 8;     // queries per task: 8 x 16 heads = 128 rows
+constexpr int kMaxTokens = 1 << 20;
+
+// Header slots (int64) in the plan workspace.
+enum HeaderSlot {
+  kHdrStatus = 0,   // OR of (1 << msa_status) for device-detected errors
+  kHdrNB = 1,       // number of 128-key blocks over all documents
+  kHdrTri = 2,      // count entries: 4 * sum_d nblk_d (nblk_d + 1) / 2
+  kHdrNnz = 3,      // CSR entries
+  kHdrTasks = 4,    // tasks
+  kHdrPairs = 5,    // attended (query, head, key) triples
+  kHdrTriPerG = 6,  // count entries per index head
+  kHdrWords = 16
+};
+
+__device__ __forceinline__ void raise_status(int64_t* header, msa_status s) {
+  atomicOr(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
+           1ull << static_cast<int>(s));
+}
+__device__ __forceinline__ bool plan_failed(const int64_t* header) {
+  return *reinterpret_cast<const volatile int64_t*>(header + kHdrStatus) != 0;
+}
+
+// Per-document record in the plan: start token, length, blocks, first global block.
+struct DocInfo {
+  int32_t start, len, nblk, blk_base;
+};
+
+// Task record (int4): x = index of the first query in col, y = first key token,
+// z = key count (1..128) | query count (1..8) << 8 | index head << 12,
+// w = sub-bucket id (tasks with equal w share the same K/V block).
+struct TaskView {
+  int32_t col_begin, key_start, key_len, nq, g, sub;
+};
+__device__ __forceinline__ TaskView decode_task(int4 t) {
+  TaskView v;
+  v.col_begin = t.x;
+  v.key_start = t.y;
+  v.key_len = t.z & 0xFF;
+  v.nq = (t.z >> 8) & 0xF;
+  v.g = (t.z >> 12) & 0x3;
+  v.sub = t.w;
+  return v;
+}
+
+// Index of count entry (g, doc, key block v, query block qb), v <= qb < n, in
+// the order (g, doc, super-block of qb, v, qb): tasks emitted in this order
+// walk one super-block of queries at a time.  Zs = super-block length in
+// query blocks (>= 1).  Returns the offset inside the (g, doc) segment.
+__host__ __device__ __forceinline__ int64_t tri_local(int64_t n, int64_t Zs, int64_t v,
+                                                      int64_t qb) {
+  const int64_t lo = (qb / Zs) * Zs;
+  const int64_t hi = (lo + Zs < n) ? lo + Zs : n;
+  const int64_t w = hi - lo;
+  const int64_t base = lo * (lo + 1) / 2;
+  int64_t offv;
+  if (v < lo)
+    offv = v * w;
+  else
+    offv = lo * w + (v - lo) * hi - (v - lo) * (v + lo - 1) / 2;
+  return base + offv + (qb - (v > lo ? v : lo));
+}
+
+// Workspace layout of a plan, shared by the size query and msa_build_plan.
+struct PlanLayout {
+  int64_t nb_cap, tri_cap, nnz_cap, task_cap, scan_tmp_len;
+  size_t off_header, off_doc_info, off_doc_tri, off_cnt, off_off, off_col, off_tcnt, off_toff,
+      off_tasks, off_scan, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline PlanLayout plan_layout(int64_t T, int32_t D) {
+  PlanLayout L{};
+  // A document with n blocks holds at least 128 (n - 1) + 1 tokens, so over
+  // D documents sum n <= D + (T - D) / 128, and sum n (n + 1) / 2 is largest
+  // with D - 1 one-token documents and one long one.
+  const int64_t x = (T - D) / kBlock + 1;
+  L.nb_cap = D + (T - D) / kBlock;
+  L.tri_cap = 4 * ((D - 1) + x * (x + 1) / 2);
+  L.nnz_cap = int64_t(kKVHeads) * kTopK * T;
+  L.task_cap = L.nnz_cap / kTaskQueries + L.tri_cap;
+  L.scan_tmp_len = (L.tri_cap + 4095) / 4096 + 64;
+  size_t o = 0;
+  L.off_header = o;   o = align_up(o + sizeof(int64_t) * kHdrWords, 256);
+  L.off_doc_info = o; o = align_up(o + sizeof(DocInfo) * D, 256);
+  L.off_doc_tri = o;  o = align_up(o + sizeof(int64_t) * (D + 1), 256);
+  L.off_cnt = o;      o = align_up(o + sizeof(int32_t) * L.tri_cap, 256);
+  L.off_off = o;      o = align_up(o + sizeof(int32_t) * L.tri_cap, 256);
+  L.off_col = o;      o = align_up(o + sizeof(int32_t) * L.nnz_cap, 256);
+  L.off_tcnt = o;     o = align_up(o + sizeof(int32_t) * L.tri_cap, 256);
+  L.off_toff = o;     o = align_up(o + sizeof(int32_t) * L.tri_cap, 256);
+  L.off_tasks = o;    o = align_up(o + sizeof(int4) * L.task_cap, 256);
+  L.off_scan = o;     o = align_up(o + sizeof(int32_t) * L.scan_tmp_len, 256);
+  L.total = o;
+  return L;
+}
+
+// Kernel-launch bookkeeping (profiling hooks, launch counter) - msa_api.cu.
+// launch_end counts `kernels` launches under `name`.
+void launch_begin(const char* name, cudaStream_t s);
+void launch_end(const char* name, cudaStream_t s, int kernels = 1);
+
+// Launchers implemented in the kernel translation units.
+cudaError_t launch_plan(const msa_plan& p, cudaStream_t s);
+cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, const void* v,
+                           float scale, void* o, float* lse, void* ws, cudaStream_t s);
+cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, float scale,
+                            void* dq, void* dk, void* dv, void* ws, cudaStream_t s);
+size_t forward_workspace_bytes(const msa_plan& p);
+size_t backward_workspace_bytes(const msa_plan& p);
+
+}  // namespace msa

@@ -1,0 +1,356 @@
+// plan.cu - device-side plan builder: q2k -> k2q CSR -> task table.
+//
+// The pages describe this step as the official CSR builder plus the fused
+// task builder that "keeps exact counts and CTA scheduling on the device"
+// (NeMo-Automodel PR "feat(minimax-m3) ...", Changelog; API page
+// msa_backward_sm100: task rows of 8 queries x 16 main heads bucketed by
+// (batch, index_head, key_block)).  Everything here stays on the device and
+// is launched with capacity-bounded grids; exact counts are read from the
+// plan header.
+//
+// Count entries.  For index head g, document d (n blocks), key block v and
+// query block qb >= v, entry (g, d, v, qb) counts the queries of block qb that
+// selected v.  Entries are ordered (g, d, super-block of qb, v, qb) - see
+// tri_local - so one exclusive scan gives each entry its place in col, queries
+// end up ascending within every bucket, and the task table comes out grouped
+// by super-block.  A CTA per (g, d, qb) builds a 128-query bitmap per key
+// block in shared memory: popcounts give the counts, prefix popcounts give
+// each query's rank, and duplicate slots collapse for free.
+#include "common.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 4;
+constexpr int kScanTile = kScanThreads * kScanItems;  // elements per scan CTA
+constexpr int kChunkV = 1024;                         // key blocks per bitmap pass
+
+// ------------------------------------------------------------ block scans
+template <typename Tv>
+__device__ __forceinline__ Tv warp_incl_scan(Tv x) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    Tv y = __shfl_up_sync(0xffffffffu, x, o);
+    if ((threadIdx.x & 31) >= o) x += y;
+  }
+  return x;
+}
+
+// Exclusive scan over the CTA (blockDim.x == 1024); returns the prefix of x
+// and writes the CTA total to *total.
+template <typename Tv>
+__device__ Tv block_excl_scan(Tv x, Tv* total) {
+  __shared__ Tv warp_tot[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  Tv inc = warp_incl_scan(x);
+  if (lane == 31) warp_tot[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    Tv v = warp_tot[lane];
+    Tv vi = warp_incl_scan(v);
+    warp_tot[lane] = vi - v;
+    if (lane == 31) *total = vi;
+  }
+  __syncthreads();
+  Tv res = inc - x + (w == 0 ? Tv(0) : warp_tot[w]);
+  __syncthreads();
+  return res;
+}
+
+// ------------------------------------------------------------ documents
+__global__ void __launch_bounds__(1024) k_plan_docs(msa_plan p) {
+  __shared__ int bad;
+  __shared__ int64_t tot_nb, tot_tri;
+  const int32_t* offs = p.doc_offsets;
+  const int D = p.num_docs;
+  int64_t* hdr = p.header;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kHdrWords; ++i) hdr[i] = 0;
+    bad = (offs[0] != 0 || int64_t(offs[D]) != p.T);
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += blockDim.x)
+    if (offs[d + 1] <= offs[d]) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) raise_status(hdr, MSA_ERR_BAD_OFFSETS);
+    return;
+  }
+  DocInfo* info = reinterpret_cast<DocInfo*>(p.doc_info);
+  int64_t carry_nb = 0, carry_tri = 0;
+  for (int base = 0; base < D; base += blockDim.x) {
+    const int d = base + threadIdx.x;
+    int64_t nb = 0, start = 0, len = 0;
+    if (d < D) {
+      start = offs[d];
+      len = int64_t(offs[d + 1]) - start;
+      nb = (len + kBlock - 1) / kBlock;
+    }
+    const int64_t tri = nb * (nb + 1) / 2;
+    const int64_t ex_nb = block_excl_scan<int64_t>(nb, &tot_nb);
+    const int64_t ex_tri = block_excl_scan<int64_t>(tri, &tot_tri);
+    if (d < D) {
+      info[d] = DocInfo{int32_t(start), int32_t(len), int32_t(nb), int32_t(carry_nb + ex_nb)};
+      p.doc_tri[d] = carry_tri + ex_tri;
+    }
+    __syncthreads();
+    carry_nb += tot_nb;
+    carry_tri += tot_tri;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.doc_tri[D] = carry_tri;
+    if (4 * carry_tri > p.tri_cap || carry_nb > p.nb_cap) {
+      raise_status(hdr, MSA_ERR_CAPACITY);
+      return;
+    }
+    hdr[kHdrNB] = carry_nb;
+    hdr[kHdrTriPerG] = carry_tri;
+    hdr[kHdrTri] = 4 * carry_tri;
+  }
+}
+
+// ------------------------------------------------------------ per query block
+enum BlockPass { kPassCount = 0, kPassScatter = 1, kPassEmit = 2 };
+
+template <int PASS>
+__global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
+  __shared__ uint32_t bm[kChunkV][4];
+  __shared__ int s_doc, s_skip;
+  __shared__ unsigned long long s_pairs;
+  int64_t* hdr = p.header;
+  const int64_t NB = hdr[kHdrNB];
+  const int g = int(blockIdx.x / p.nb_cap);
+  const int64_t gb = int64_t(blockIdx.x % p.nb_cap);
+  if (gb >= NB) return;
+  const DocInfo* info = reinterpret_cast<const DocInfo*>(p.doc_info);
+  if (threadIdx.x == 0) {
+    // Read once and broadcast: another CTA may raise the status meanwhile.
+    s_skip = plan_failed(hdr) ? 1 : 0;
+    int lo = 0, hi = p.num_docs - 1;  // last document whose first block <= gb
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (info[mid].blk_base <= gb) lo = mid; else hi = mid - 1;
+    }
+    s_doc = lo;
+    s_pairs = 0;
+  }
+  __syncthreads();
+  if (s_skip) return;
+  const int d = s_doc;
+  const DocInfo di = info[d];
+  const int64_t n = di.nblk;
+  const int64_t qb = gb - di.blk_base;
+  const int64_t Zs = p.super_block > 0 ? p.super_block : n;
+  const int64_t seg = int64_t(g) * hdr[kHdrTriPerG] + p.doc_tri[d];
+  const int r = threadIdx.x;
+  const int64_t pos = qb * kBlock + r;
+  const bool valid = pos < di.len;
+  const int64_t t = di.start + pos;
+
+  int32_t sl[kTopK];
+  if (valid) {
+    const int4* src = reinterpret_cast<const int4*>(p.q2k + (int64_t(g) * p.T + t) * kTopK);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int4 x = src[i];
+      sl[4 * i + 0] = x.x; sl[4 * i + 1] = x.y; sl[4 * i + 2] = x.z; sl[4 * i + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kTopK; ++i) sl[i] = -1;
+  }
+  if (PASS == kPassCount && valid) {
+#pragma unroll
+    for (int i = 0; i < kTopK; ++i)
+      if (sl[i] < -1 || sl[i] >= n) raise_status(hdr, MSA_ERR_BAD_Q2K);
+  }
+  // A slot counts once: later duplicates of a value are dropped.
+#pragma unroll
+  for (int i = 1; i < kTopK; ++i)
+#pragma unroll
+    for (int j = 0; j < i; ++j)
+      if (sl[i] == sl[j]) sl[i] = -1;
+
+  const int64_t lo_q = (qb / Zs) * Zs;       // first query block of this super-block
+  const int64_t hi_q = lo_q + Zs < n ? lo_q + Zs : n;
+  int64_t pairs = 0;
+
+  for (int64_t c0 = 0; c0 <= qb; c0 += kChunkV) {
+    const int64_t cend = (c0 + kChunkV - 1 < qb) ? c0 + kChunkV - 1 : qb;
+    const int span = int(cend - c0 + 1);
+    for (int i = threadIdx.x; i < span * 4; i += blockDim.x) (&bm[0][0])[i] = 0u;
+    __syncthreads();
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i)
+        if (sl[i] >= c0 && sl[i] <= cend) atomicOr(&bm[sl[i] - c0][r >> 5], 1u << (r & 31));
+    }
+    __syncthreads();
+    if (PASS == kPassCount) {
+      for (int64_t v = c0 + threadIdx.x; v <= cend; v += blockDim.x) {
+        const uint32_t* b = bm[v - c0];
+        p.cnt[seg + tri_local(n, Zs, v, qb)] =
+            __popc(b[0]) + __popc(b[1]) + __popc(b[2]) + __popc(b[3]);
+      }
+    } else if (PASS == kPassScatter) {
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < kTopK; ++i) {
+          const int64_t v = sl[i];
+          if (v < c0 || v > cend) continue;
+          const uint32_t* b = bm[v - c0];
+          const int w = r >> 5;
+          int rank = __popc(b[w] & ((1u << (r & 31)) - 1u));
+          for (int k = 0; k < w; ++k) rank += __popc(b[k]);
+          p.col[p.off[seg + tri_local(n, Zs, v, qb)] + rank] = int32_t(t);
+          pairs += (v < qb) ? kBlock : (pos - qb * kBlock + 1);
+        }
+      }
+      // Tasks per sub-bucket: the run of entries (v, qb') for qb' in
+      // [max(v, lo_q), hi_q) is contiguous; its head entry owns the tasks.
+      for (int64_t v = c0 + threadIdx.x; v <= cend; v += blockDim.x) {
+        const int64_t e = seg + tri_local(n, Zs, v, qb);
+        const int64_t first = v > lo_q ? v : lo_q;
+        if (qb == first) {
+          const int64_t last = e + (hi_q - first) - 1;
+          const int64_t len = int64_t(p.off[last]) + p.cnt[last] - p.off[e];
+          p.tcnt[e] = int32_t((len + kTaskQueries - 1) / kTaskQueries);
+        } else {
+          p.tcnt[e] = 0;
+        }
+      }
+    } else {  // kPassEmit
+      // Heads in this CTA: v == qb, and every v < lo_q when qb == lo_q.
+      const int64_t vbeg = (qb == lo_q) ? c0 : (qb >= c0 ? qb : cend + 1);
+      for (int64_t v = vbeg; v <= cend; ++v) {
+        if (qb != lo_q && v != qb) continue;
+        if (qb == lo_q && v > qb) continue;
+        const int64_t first = v > lo_q ? v : lo_q;
+        const int64_t e = seg + tri_local(n, Zs, v, qb);
+        const int64_t last = e + (hi_q - first) - 1;
+        const int64_t len = int64_t(p.off[last]) + p.cnt[last] - p.off[e];
+        const int nt = p.tcnt[e];
+        const int32_t key_start = int32_t(di.start + v * kBlock);
+        const int32_t key_len = int32_t(di.len - v * kBlock < kBlock ? di.len - v * kBlock : kBlock);
+        for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+          const int64_t rem = len - int64_t(i) * kTaskQueries;
+          const int32_t nq = int32_t(rem < kTaskQueries ? rem : kTaskQueries);
+          int4 task;
+          task.x = p.off[e] + i * kTaskQueries;
+          task.y = key_start;
+          task.z = key_len | (nq << 8) | (g << 12);
+          task.w = int32_t(e);
+          reinterpret_cast<int4*>(p.tasks)[p.toff[e] + i] = task;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (PASS == kPassScatter) {
+    if (pairs) atomicAdd(&s_pairs, (unsigned long long)pairs);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_pairs)
+      atomicAdd(reinterpret_cast<unsigned long long*>(hdr + kHdrPairs),
+                s_pairs * (unsigned long long)kHeadsPerGroup);
+  }
+}
+
+// ------------------------------------------------------------ device scan
+// Exclusive scan of in[0, n) -> out, n read from the device; the total goes to
+// *total.  Three launches, grids sized by capacity.
+__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(const int32_t* in, const int64_t* n_ptr,
+                                                              int32_t* sums) {
+  __shared__ int64_t tot;
+  const int64_t n = *n_ptr;
+  const int64_t base = int64_t(blockIdx.x) * kScanTile;
+  if (base >= n) return;
+  int64_t s = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t j = base + int64_t(threadIdx.x) * kScanItems + i;
+    if (j < n) s += in[j];
+  }
+  block_excl_scan<int64_t>(s, &tot);
+  if (threadIdx.x == 0) sums[blockIdx.x] = int32_t(tot);
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_sums(int32_t* sums, const int64_t* n_ptr,
+                                                            int64_t* total) {
+  __shared__ int64_t tot;
+  const int64_t n = *n_ptr;
+  const int64_t nb = (n + kScanTile - 1) / kScanTile;
+  int64_t carry = 0;
+  for (int64_t base = 0; base < nb; base += blockDim.x) {
+    const int64_t j = base + threadIdx.x;
+    const int64_t x = j < nb ? sums[j] : 0;
+    const int64_t ex = block_excl_scan<int64_t>(x, &tot);
+    if (j < nb) sums[j] = int32_t(carry + ex);
+    carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *total = carry;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_down(const int32_t* in, int32_t* out,
+                                                            const int64_t* n_ptr,
+                                                            const int32_t* sums) {
+  __shared__ int64_t tot;
+  const int64_t n = *n_ptr;
+  const int64_t base = int64_t(blockIdx.x) * kScanTile;
+  if (base >= n) return;
+  int32_t v[kScanItems];
+  int64_t s = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t j = base + int64_t(threadIdx.x) * kScanItems + i;
+    v[i] = j < n ? in[j] : 0;
+    s += v[i];
+  }
+  int64_t run = block_excl_scan<int64_t>(s, &tot) + sums[blockIdx.x];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t j = base + int64_t(threadIdx.x) * kScanItems + i;
+    if (j < n) out[j] = int32_t(run);
+    run += v[i];
+  }
+}
+
+cudaError_t scan(const int32_t* in, int32_t* out, const int64_t* n_ptr, int64_t cap,
+                 int32_t* tmp, int64_t* total, cudaStream_t s) {
+  const unsigned grid = unsigned((cap + kScanTile - 1) / kScanTile);
+  if (grid == 0) return cudaSuccess;
+  launch_begin("plan_scan", s);
+  k_scan_reduce<<<grid, kScanThreads, 0, s>>>(in, n_ptr, tmp);
+  k_scan_sums<<<1, kScanThreads, 0, s>>>(tmp, n_ptr, total);
+  k_scan_down<<<grid, kScanThreads, 0, s>>>(in, out, n_ptr, tmp);
+  launch_end("plan_scan", s, 3);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const msa_plan& p, cudaStream_t s) {
+  launch_begin("plan_docs", s);
+  k_plan_docs<<<1, 1024, 0, s>>>(p);
+  launch_end("plan_docs", s);
+  const unsigned grid = unsigned(4 * p.nb_cap);
+  launch_begin("plan_count", s);
+  k_plan_blocks<kPassCount><<<grid, 128, 0, s>>>(p);
+  launch_end("plan_count", s);
+  cudaError_t e = scan(p.cnt, p.off, p.header + kHdrTri, p.tri_cap, p.scan_tmp,
+                       p.header + kHdrNnz, s);
+  if (e != cudaSuccess) return e;
+  launch_begin("plan_scatter", s);
+  k_plan_blocks<kPassScatter><<<grid, 128, 0, s>>>(p);
+  launch_end("plan_scatter", s);
+  e = scan(p.tcnt, p.toff, p.header + kHdrTri, p.tri_cap, p.scan_tmp, p.header + kHdrTasks, s);
+  if (e != cudaSuccess) return e;
+  launch_begin("plan_emit", s);
+  k_plan_blocks<kPassEmit><<<grid, 128, 0, s>>>(p);
+  launch_end("plan_emit", s);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

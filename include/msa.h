@@ -1,0 +1,204 @@
+/*
+ * msa.h - C ABI of libmsa: block-sparse, causal, document-local grouped-query
+ * attention (MiniMax Sparse Attention, "MSA") forward and backward on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes is fixed by the flat-attention interface of the
+ * NeMo-Automodel PR "feat(minimax-m3): add SM100 MSA sparse attention with
+ * custom backward" (sections "Design" and "Supported scope") and by the
+ * run_backward contract on the API page "msa_backward_sm100":
+ *
+ *   Q, dO : bf16 [T, 64, 128]   compact token-major (THD) rows
+ *   K, V  : bf16 [T, 4, 128]
+ *   q2k   : int32 [4, T, 16]    document-local key-block ids per index head,
+ *                               -1 marks an unused slot
+ *   doc_offsets : int32 [D+1]   0 = o_0 < o_1 < ... < o_D = T
+ *
+ * Query head h reads KV head and index head g = h / 16.  Token t = o_d + p of
+ * document d attends key o_d + j iff j <= p and floor(j / 128) is one of the
+ * values in q2k[g, t, :] (a set: duplicates count once).  Then
+ *   s_j = scale * <Q[t,h], K[j,g]>,  LSE[t,h] = ln sum_j exp(s_j),
+ *   O[t,h] = sum_j exp(s_j - LSE[t,h]) V[j,g],
+ * and the backward returns dQ, dK, dV of L = sum(O * dO).  A row that sees no
+ * key gets O = 0, LSE = -inf and zero gradients.  A q2k value < -1 or >= the
+ * document's block count is an error (MSA_ERR_BAD_Q2K, detected on device).
+ *
+ * Conventions for every call:
+ *   - All tensor and workspace pointers are DEVICE pointers on the current
+ *     CUDA device, contiguous, 16-byte aligned.  The caller owns all memory;
+ *     the library never allocates or frees device memory.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronise, except the diagnostics
+ *     msa_read_status and msa_plan_export which say so.
+ *   - Host-detectable problems (null pointer, bad size, misalignment, small
+ *     workspace) return an error before anything is launched.  Problems only
+ *     the device can see (bad q2k value, bad document offsets, a pipeline
+ *     wait that timed out) set bits of the plan's device status word; later
+ *     kernels of the same plan then skip their work.  msa_read_status reads it.
+ *   - Gradients are accumulated with floating-point atomics, so results are
+ *     not bitwise reproducible from run to run.  There is no deterministic
+ *     mode.
+ *   - Limits: 1 <= T <= 2^25, 1 <= num_docs <= T.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Stream handle: a cudaStream_t, passed as an opaque pointer. */
+typedef struct CUstream_st* msa_stream_t;
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* null pointer, T or num_docs out of range, ...  */
+  MSA_ERR_UNSUPPORTED = 2,  /* device is not sm_100 / sm_103 class             */
+  MSA_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned                */
+  MSA_ERR_WORKSPACE = 4,    /* workspace smaller than the *_workspace_bytes   */
+  MSA_ERR_CUDA = 5,         /* a CUDA runtime call failed                      */
+  MSA_ERR_BAD_Q2K = 6,      /* device: a q2k slot outside [-1, blocks of doc)  */
+  MSA_ERR_BAD_OFFSETS = 7,  /* device: doc_offsets not 0 < ... strictly up .. T */
+  MSA_ERR_TIMEOUT = 8,      /* device: a bounded pipeline wait gave up         */
+  MSA_ERR_CAPACITY = 9      /* device: a plan table exceeded its capacity      */
+} msa_status;
+
+/* Human-readable name of a status code (static string). */
+const char* msa_status_string(msa_status s);
+
+/* Plan-build options.  Pass NULL for the defaults. */
+typedef struct msa_plan_options {
+  /* Tasks of one (index head, key block) bucket are cut at runs of
+   * super_block consecutive query blocks (0 = never cut).  Default 16. */
+  int32_t super_block;
+  int32_t reserved[7];
+} msa_plan_options;
+
+/*
+ * The execution plan derived from q2k and the document layout: per index
+ * head and key block, the queries that selected it (the k2q CSR), and the
+ * task table of 128-row tiles (8 queries x 16 heads of one index head against
+ * one key block) that the forward and backward kernels walk.  The pages call
+ * these the CSR / scheduler metadata and the backward task rows
+ * (msa_backward_sm100: "task rows (8 queries x 16 main heads = one 128-row
+ * tile) bucketed by (batch, index_head, key_block)").
+ *
+ * A plain struct of device pointers into the caller's plan workspace and of
+ * host-side capacities.  Fill it with msa_build_plan; do not edit it.  It
+ * stays valid while the workspace and the q2k / doc_offsets buffers live and
+ * may be reused by any number of msa_forward / msa_backward calls on the same
+ * T, q2k and documents.  All counts live on the device.
+ */
+typedef struct msa_plan {
+  int64_t T;
+  int32_t num_docs;
+  int32_t super_block;
+  int64_t nb_cap;     /* bound on the number of 128-key blocks            */
+  int64_t tri_cap;    /* bound on (index head, doc, key block, query block) */
+  int64_t nnz_cap;    /* bound on CSR entries                              */
+  int64_t task_cap;   /* bound on tasks                                    */
+  const int32_t* q2k;
+  const int32_t* doc_offsets;
+  int64_t* header;    /* device: status and counts                         */
+  int32_t* doc_info;  /* device: [num_docs][4] start, length, blocks, block base */
+  int64_t* doc_tri;   /* device: [num_docs+1] prefix of per-doc count entries */
+  int32_t* cnt;       /* device: [tri_cap] queries per count entry          */
+  int32_t* off;       /* device: [tri_cap] exclusive prefix of cnt          */
+  int32_t* col;       /* device: [nnz_cap] query tokens, sorted per entry   */
+  int32_t* tcnt;      /* device: [tri_cap] tasks per count entry            */
+  int32_t* toff;      /* device: [tri_cap] exclusive prefix of tcnt         */
+  int32_t* tasks;     /* device: [task_cap][4] task records                 */
+  int32_t* scan_tmp;  /* device: scan scratch                               */
+  int64_t scan_tmp_len;
+} msa_plan;
+
+/* Bytes of plan workspace needed for T tokens in num_docs documents.
+ * Host only, no CUDA call. */
+msa_status msa_plan_workspace_bytes(int64_t T, int32_t num_docs, size_t* bytes);
+
+/*
+ * Build the plan on the device (no host synchronisation): validate the
+ * document offsets and q2k, invert q2k into the k2q CSR (queries ascending
+ * within each bucket), cut the buckets into tasks and count the attended
+ * (query, head, key) triples.
+ *   q2k          device int32 [4, T, 16]
+ *   doc_offsets  device int32 [num_docs + 1]
+ *   workspace    device, >= msa_plan_workspace_bytes(T, num_docs)
+ *   out          host struct, filled on success
+ * Device-side validation failures set MSA_ERR_BAD_Q2K / MSA_ERR_BAD_OFFSETS in
+ * the status word (see msa_read_status); forward and backward then do no work.
+ */
+msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_t T,
+                          int32_t num_docs, const msa_plan_options* opts, void* workspace,
+                          size_t workspace_bytes, msa_stream_t stream, msa_plan* out);
+
+/* Bytes of forward workspace for a plan (host only). */
+msa_status msa_forward_workspace_bytes(const msa_plan* plan, size_t* bytes);
+
+/*
+ * Forward (the pages' "flat sparse forward": O [T,64,128] and LSE [T,64]).
+ *   q  device bf16 [T,64,128]; k, v device bf16 [T,4,128]
+ *   softmax_scale   e.g. 1/sqrt(128)
+ *   o   device bf16 [T,64,128] (written)
+ *   lse device fp32 [T,64] natural-log LSE (written; -inf for keyless rows)
+ *   workspace device, >= msa_forward_workspace_bytes(plan)
+ */
+msa_status msa_forward(const msa_plan* plan, const void* q, const void* k, const void* v,
+                       float softmax_scale, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, msa_stream_t stream);
+
+/* Bytes of backward workspace for a plan (host only). */
+msa_status msa_backward_workspace_bytes(const msa_plan* plan, size_t* bytes);
+
+/*
+ * Backward (the pages' launch sequence: delta = rowsum(dO * O) -> zero the
+ * gradient pools -> main KV-parallel backward -> BF16 finalize), see
+ * msa_backward_sm100 run_backward.  O and LSE are the forward's outputs.
+ *   dq device bf16 [T,64,128]; dk, dv device bf16 [T,4,128] (written; compact
+ *   token order, zero for rows that receive no gradient)
+ */
+msa_status msa_backward(const msa_plan* plan, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout, float softmax_scale,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        msa_stream_t stream);
+
+/* Synchronises the stream and returns the plan's device status (MSA_OK if no
+ * device-side error was recorded).  For tests and diagnostics. */
+msa_status msa_read_status(const msa_plan* plan, msa_stream_t stream);
+
+/* Plan counts after synchronising the stream: counts[0] = key blocks NB,
+ * [1] = CSR entries, [2] = tasks, [3] = attended (query, head, key) triples,
+ * [4] = count entries.  Host array of 5 int64. */
+msa_status msa_plan_counts(const msa_plan* plan, msa_stream_t stream, int64_t* counts);
+
+/*
+ * Copy the plan tables to host memory after synchronising the stream (for
+ * the bit-exact plan tests).  Each destination may be NULL to skip it.
+ *   col   int32 [nnz]  query tokens, grouped by task order
+ *   tasks int32 [ntasks][4]: {first col index, first key token,
+ *         key count | query count << 8 | index head << 12, sub-bucket id}
+ * Capacities are element counts; too small -> MSA_ERR_INVALID_ARG.
+ */
+msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* col,
+                           int64_t col_capacity, int32_t* tasks, int64_t task_capacity);
+
+/*
+ * Kernel timing for benchmarks.  While enabled, every kernel the library
+ * launches is bracketed by CUDA events on its launch stream.  msa_profile_read
+ * synchronises and returns, for the kernel family named (e.g. "fwd_main",
+ * "bwd_main"), the launch count and the summed device time since the last
+ * reset.  msa_launch_count returns the number of kernels the library has
+ * launched since it was loaded.
+ */
+msa_status msa_profile_enable(int32_t on);
+msa_status msa_profile_reset(void);
+msa_status msa_profile_read(const char* name, int64_t* launches, double* total_ms);
+int64_t msa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H_ */

@@ -202,3 +202,14 @@ def plan(q2k, doc_offsets, T: int, super_block: int = 16, lib=None):
         "row_ptr": row_ptr[: 4 * NB + 1].copy(), "col": col[:nnz].copy(),
         "tasks": tasks[:nt].copy(),
     }
+
+
+def pair_count(q2k, doc_offsets, T: int) -> int:
+    """Attended (query, head, key) triples of a selection (the FLOP-count basis)."""
+    lib = _load()
+    q2k = _i32(q2k)
+    offs = _i32(doc_offsets)
+    n = lib.oracle_pair_count(_ptr(q2k), T, _ptr(offs), offs.size - 1)
+    if n < 0:
+        raise OracleError("pair_count: invalid input")
+    return int(n)

@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: libmsa.so builds and loads, exports every function
+include/msa.h declares, and rejects bad arguments on the host before any
+launch."""
+import ctypes
+import re
+
+import pytest
+
+from block_sparse_gqa_msa_gb300 import api
+from block_sparse_gqa_msa_gb300 import build as msa_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    msa_build.build()
+    return api.lib()
+
+
+def declared_functions():
+    text = open(api.HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(api.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code, name in api.STATUS.items():
+        assert lib.msa_status_string(code).decode() == name
+
+
+def test_workspace_bytes_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.msa_plan_workspace_bytes(16384, 10, ctypes.byref(n)) == 0 and n.value > 0
+    small = n.value
+    assert lib.msa_plan_workspace_bytes(131072, 1, ctypes.byref(n)) == 0 and n.value > small
+    for T, D in ((0, 1), (-5, 1), (1 << 21, 1), (100, 0), (100, 101)):
+        assert lib.msa_plan_workspace_bytes(T, D, ctypes.byref(n)) == 1
+    assert lib.msa_plan_workspace_bytes(100, 1, None) == 1
+
+
+def test_build_plan_host_checks(lib):
+    st = api.MsaPlanStruct()
+    ws_n = ctypes.c_size_t(0)
+    lib.msa_plan_workspace_bytes(1000, 2, ctypes.byref(ws_n))
+    good = ctypes.c_void_p(0x10000)
+    opts = api.MsaPlanOptions(super_block=16)
+    # null pointers
+    assert lib.msa_build_plan(None, good, 1000, 2, None, good, ws_n.value, None,
+                              ctypes.byref(st)) == 1
+    assert lib.msa_build_plan(good, good, 1000, 2, None, good, ws_n.value, None, None) == 1
+    # sizes
+    assert lib.msa_build_plan(good, good, 0, 2, None, good, ws_n.value, None,
+                              ctypes.byref(st)) == 1
+    bad_opts = api.MsaPlanOptions(super_block=-1)
+    assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(bad_opts), good, ws_n.value, None,
+                              ctypes.byref(st)) == 1
+    # alignment
+    assert lib.msa_build_plan(ctypes.c_void_p(0x10004), good, 1000, 2, ctypes.byref(opts), good,
+                              ws_n.value, None, ctypes.byref(st)) == 3
+    # workspace too small
+    assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(opts), good, ws_n.value - 1, None,
+                              ctypes.byref(st)) == 4
+
+
+def test_forward_backward_host_checks(lib):
+    st = api.MsaPlanStruct()
+    g = ctypes.c_void_p(0x10000)
+    assert lib.msa_forward(None, g, g, g, 0.1, g, g, g, 1 << 30, None) == 1
+    assert lib.msa_backward(None, g, g, g, g, g, g, 0.1, g, g, g, g, 1 << 30, None) == 1
+    st.T, st.num_docs = 100, 1
+    st.header, st.tasks = 0x10000, 0x20000
+    ref = ctypes.byref(st)
+    assert lib.msa_forward(ref, None, g, g, 0.1, g, g, g, 1 << 30, None) == 1
+    assert lib.msa_forward(ref, g, g, g, -1.0, g, g, g, 1 << 30, None) == 1
+    assert lib.msa_forward(ref, ctypes.c_void_p(0x10008), g, g, 0.1, g, g, g, 1 << 30, None) == 3
+    assert lib.msa_forward(ref, g, g, g, 0.1, g, g, g, 16, None) == 4
+    assert lib.msa_backward(ref, g, g, g, g, g, g, 0.1, g, g, ctypes.c_void_p(0x10002), g,
+                            1 << 30, None) == 3
+    n = ctypes.c_size_t(0)
+    assert lib.msa_forward_workspace_bytes(ref, ctypes.byref(n)) == 0 and n.value >= 100 * 64 * 128 * 4
+    assert lib.msa_backward_workspace_bytes(ref, ctypes.byref(n)) == 0 and n.value >= 100 * 64 * 128 * 4
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q2k = torch.zeros(4, 10, 16, dtype=torch.int32)
+    offs = torch.tensor([0, 10], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        api.msa_build_plan(q2k, offs)
