@@ -1,0 +1,366 @@
+"""Benchmark: MSA forward + backward on the packed-document T=16384 workload.
+
+One step = the whole hot path on one batch: plan build (q2k -> CSR -> tasks),
+forward (O, LSE) and backward (dQ, dK, dV), inputs resident in HBM.  L2 is
+flushed (256 MiB write) before every timed step; each step is bracketed by
+CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  FLOPs are the method's own: 4*d per attended
+(query, head, key) triple forward and 10*d backward, counted exactly by the
+plan builder.  Under torchrun (N > 1) every rank runs its own replica of the
+workload (weak scaling, no data-path collective); rank 0 prints the
+aggregate.  ``--impl reference`` times the fp64 CPU oracle (the reference arm)
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_gqa_msa_gb300 import inputs  # noqa: E402
+
+HEAD_DIM = 128
+FWD_FLOP_PER_PAIR = 4 * HEAD_DIM
+BWD_FLOP_PER_PAIR = 10 * HEAD_DIM
+METRIC = "MSA fwd+bwd sparse TFLOP/s & tokens/s at T=16k; % of GB300 BF16 tensor peak"
+WORKLOAD = 3  # packed 16k row of documents
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"msa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm
+def cpu_sample(w, budget_s: float = 20.0):
+    """Time the fp64 oracle's forward + backward on whole documents of the
+    workload (documents are independent, so each is a faithful sample)."""
+    import oracle
+    offs = w.doc_offsets.numpy()
+    lens = np.diff(offs)
+    order = np.argsort(np.abs(lens - np.median(lens)))  # typical documents first
+    flops = 0.0
+    pairs_total = 0
+    spent = 0.0
+    used = []
+    for d in order:
+        s, e = int(offs[d]), int(offs[d + 1])
+        sub = inputs.Workload(
+            name="doc", q=w.q[s:e], k=w.k[s:e], v=w.v[s:e], do=w.do[s:e],
+            q2k=w.q2k[:, s:e].contiguous(),
+            doc_offsets=torch.tensor([0, e - s], dtype=torch.int32), scale=w.scale)
+        P = oracle.Problem.from_workload(sub)
+        pairs = P.pair_count()
+        t0 = time.perf_counter()
+        P.forward()
+        P.backward()
+        dt = time.perf_counter() - t0
+        spent += dt
+        pairs_total += pairs
+        flops += pairs * (FWD_FLOP_PER_PAIR + BWD_FLOP_PER_PAIR)
+        used.append(e - s)
+        if spent >= budget_s * 0.5:
+            break
+    return {
+        "flops": flops, "seconds": spent, "tokens": int(sum(used)), "docs": len(used),
+        "pairs": pairs_total, "cores": oracle.threads(),
+        "sample": f"{len(used)} whole document(s) ({sum(used)} tokens, lengths {used}) of the "
+                  f"packed T=16384 row: oracle forward + backward in fp64",
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = inputs.config(WORKLOAD)
+    budget = max(3.0, 30.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_sample(w, budget)
+    times, flops, last = [], 0.0, None
+    for _ in range(args.steps):
+        last = cpu_sample(w, budget)
+        times.append(last["seconds"])
+        flops += last["flops"]
+    total = sum(times)
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "docs": w.num_docs},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"],
+                         "kind": "oracle", "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    from block_sparse_gqa_msa_gb300 import api
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = inputs.config(WORKLOAD, seed=inputs.CONFIG_SEEDS[WORKLOAD] + rank)
+    T = w.T
+    stream = torch.cuda.current_stream()
+    q, k, v, do = (x.to(dev) for x in (w.q, w.k, w.v, w.do))
+    q2k, offs = w.q2k.to(dev), w.doc_offsets.to(dev)
+    plan = api.msa_build_plan(q2k, offs, super_block=args.super_block)
+    pws = plan.workspace
+    fws = torch.empty(api.forward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    bws = torch.empty(api.backward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((T, 64), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, workspace=pws)
+        api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
+        api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
+        return p
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.msa_read_status(plan) != 0:
+        raise RuntimeError(f"device status {api.msa_read_status(plan)}")
+    counts = api.msa_plan_counts(plan)
+    pairs = counts["pairs"]
+    flop_fwd = pairs * FWD_FLOP_PER_PAIR
+    flop_bwd = pairs * BWD_FLOP_PER_PAIR
+
+    # ---- device-timed loop (inputs resident, L2 flushed before each step)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler() if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    api.profile_enable(True)
+    api.profile_reset()
+    launches0 = api.launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        e = evs[i]
+        e[0].record(stream)
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, workspace=pws)
+        e[1].record(stream)
+        api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
+        e[2].record(stream)
+        api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    launches = api.launch_count() - launches0
+    clk = clocks.stop() if clocks else None
+    kern = {}
+    for name in ("plan_docs", "plan_count", "plan_scan", "plan_scatter", "plan_emit", "fwd_kmax",
+                 "fwd_rows", "fwd_main", "fwd_finalize", "fwd_fallback", "bwd_delta", "bwd_main",
+                 "bwd_finalize"):
+        n, ms = api.profile_read(name)
+        if n:
+            kern[name] = {"launches": n, "ms_per_step": ms / args.steps}
+    api.profile_enable(False)
+    if world > 1:
+        torch.distributed.barrier()
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [a + b + c for a, b, c in zip(plan_ms, fwd_ms, bwd_ms)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flop_step = flop_fwd + flop_bwd
+    value = world * flop_step / (ms_per_step * 1e-3) / 1e12
+    tok_s = world * T / (ms_per_step * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda x: x.pin_memory()  # noqa: E731
+    hq, hk, hv, hdo, hq2k, hoffs = (pin(x) for x in (w.q, w.k, w.v, w.do, w.q2k, w.doc_offsets))
+    ho, hlse = pin(torch.empty_like(w.q)), pin(torch.empty((T, 64), dtype=torch.float32))
+    hdq, hdk, hdv = pin(torch.empty_like(w.q)), pin(torch.empty_like(w.k)), pin(torch.empty_like(w.v))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hq2k, hoffs))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+    e2e_steps = max(3, args.steps // 2)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        q2k.copy_(hq2k, non_blocking=True)
+        offs.copy_(hoffs, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flop_step / (e2e_ms * 1e-3) / 1e12
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    dom = max(("fwd_main", "bwd_main"), key=lambda n: kern.get(n, {}).get("ms_per_step", 0.0))
+    dom_flop = flop_fwd if dom == "fwd_main" else flop_bwd
+    per_launch_ms = kern[dom]["ms_per_step"] * args.steps / kern[dom]["launches"]
+    achieved = dom_flop / (per_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic_path = os.path.join(ROOT, "profiles", f"{dom}_traffic.json")
+    traffic = None
+    if os.path.exists(traffic_path):
+        with open(traffic_path) as f:
+            tj = json.load(f)
+        if tj.get("workload") == w.name:
+            traffic = tj.get("bytes_per_launch")
+
+    cpu = cpu_sample(w, budget_s=20.0) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "docs": w.num_docs, "heads": "64q/4kv/4idx",
+                   "head_dim": 128, "block": 128, "topk": 16, "super_block": args.super_block,
+                   "pairs": pairs, "flop_per_step": flop_step,
+                   "l2": "flushed before each timed step (256 MiB write)"},
+        "tokens_per_s": tok_s,
+        "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_sustained_peak": 100.0 * value / world / float(peaks["bf16_tflops_sustained"]),
+        "ms": {"plan": statistics.mean(plan_ms), "fwd": statistics.mean(fwd_ms),
+               "bwd": statistics.mean(bwd_ms)},
+        "kernels_ms_per_step": {k_: round(v_["ms_per_step"], 4) for k_, v_ in kern.items()},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s"},
+    }
+    if cpu:
+        line["cpu_baseline"] = {"value": cpu["flops"] / cpu["seconds"] / 1e12, "unit": "TFLOP/s",
+                                "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--super-block", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group(backend="gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -383,8 +383,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int k0 = c * 32 + j;
           float x0 = (k0 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j]), prm.c2, -m2)) : 0.f;
           float x1 = (k0 + 1 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j + 1]), prm.c2, -m2)) : 0.f;
-          lsum += x0 + x1;
-          pk[j >> 1] = pack_bf16x2(x0, x1);
+          // The row sum adds the same bf16-rounded weights the P.V product
+          // uses, so the normalised weights of a row sum to one exactly.
+          const uint32_t w2 = pack_bf16x2(x0, x1);
+          lsum += bf16_lo(w2) + bf16_hi(w2);
+          pk[j >> 1] = w2;
         }
         const uint32_t prow = sbase + kSmP + (c >> 1) * 16384 + row * 128;
 #pragma unroll

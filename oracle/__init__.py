@@ -68,6 +68,8 @@ def _bind(lib):
     lib.oracle_plan.argtypes = [_P, _I64, _P, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _I64, _P]
     lib.oracle_pair_count.argtypes = [_P, _I64, _P, _I32]
     lib.oracle_pair_count.restype = _I64
+    lib.oracle_threads.argtypes = []
+    lib.oracle_threads.restype = ctypes.c_int
     for f in ("oracle_forward", "oracle_dq", "oracle_dkv_blocks", "oracle_backward",
               "oracle_plan"):
         getattr(lib, f).restype = ctypes.c_int
@@ -213,3 +215,8 @@ def pair_count(q2k, doc_offsets, T: int) -> int:
     if n < 0:
         raise OracleError("pair_count: invalid input")
     return int(n)
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return int(_load().oracle_threads())

@@ -489,3 +489,12 @@ int64_t oracle_pair_count(const int32_t* q2k, int64_t T, const int32_t* offs, in
   }
   return total;
 }
+
+/* Number of OpenMP threads the oracle runs with. */
+int oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
