@@ -48,7 +48,8 @@ struct DocInfo {
 
 // Task record (int4): x = index of the first query in col, y = first key token,
 // z = key count (1..128) | query count (1..8) << 8 | index head << 12,
-// w = sub-bucket id (tasks with equal w share the same K/V block).
+// w = key-block id g * nb_cap + global block (tasks with equal w read the
+// same K/V block).
 struct TaskView {
   int32_t col_begin, key_start, key_len, nq, g, sub;
 };

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
           task.x = p.off[e] + i * kTaskQueries;
           task.y = key_start;
           task.z = key_len | (nq << 8) | (g << 12);
-          task.w = int32_t(e);
+          task.w = int32_t(int64_t(g) * p.nb_cap + di.blk_base + v);
           reinterpret_cast<int4*>(p.tasks)[p.toff[e] + i] = task;
         }
       }

@@ -38,7 +38,7 @@
  *   - Gradients are accumulated with floating-point atomics, so results are
  *     not bitwise reproducible from run to run.  There is no deterministic
  *     mode.
- *   - Limits: 1 <= T <= 2^25, 1 <= num_docs <= T.
+ *   - Limits: 1 <= T <= 2^20, 1 <= num_docs <= T.
  */
 #ifndef MSA_H_
 #define MSA_H_
@@ -179,7 +179,8 @@ msa_status msa_plan_counts(const msa_plan* plan, msa_stream_t stream, int64_t* c
  * the bit-exact plan tests).  Each destination may be NULL to skip it.
  *   col   int32 [nnz]  query tokens, grouped by task order
  *   tasks int32 [ntasks][4]: {first col index, first key token,
- *         key count | query count << 8 | index head << 12, sub-bucket id}
+ *         key count | query count << 8 | index head << 12,
+ *         index head * nb_cap + global key block}
  * Capacities are element counts; too small -> MSA_ERR_INVALID_ARG.
  */
 msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* col,
