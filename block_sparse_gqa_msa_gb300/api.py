@@ -40,7 +40,7 @@ class MSAError(RuntimeError):
 class MsaPlanStruct(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int64), ("num_docs", ctypes.c_int32), ("super_block", ctypes.c_int32),
-        ("nb_cap", ctypes.c_int64), ("tri_cap", ctypes.c_int64), ("nnz_cap", ctypes.c_int64),
+        ("dq_accum", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("nb_cap", ctypes.c_int64), ("tri_cap", ctypes.c_int64), ("nnz_cap", ctypes.c_int64),
         ("task_cap", ctypes.c_int64),
         ("q2k", ctypes.c_void_p), ("doc_offsets", ctypes.c_void_p), ("header", ctypes.c_void_p),
         ("doc_info", ctypes.c_void_p), ("doc_tri", ctypes.c_void_p), ("cnt", ctypes.c_void_p),
@@ -51,7 +51,11 @@ class MsaPlanStruct(ctypes.Structure):
 
 
 class MsaPlanOptions(ctypes.Structure):
-    _fields_ = [("super_block", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+    _fields_ = [("super_block", ctypes.c_int32), ("dq_accum", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
+
+
+DQ_ACCUM = {"f16": 0, "bf16": 1, "f32": 2}
 
 
 _lock = threading.Lock()
@@ -156,8 +160,10 @@ def plan_workspace_bytes(T: int, num_docs: int) -> int:
 
 
 def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 16,
-                   workspace: torch.Tensor | None = None, stream=None) -> Plan:
-    """Device-side plan from q2k int32 [4,T,16] and doc_offsets int32 [D+1]."""
+                   workspace: torch.Tensor | None = None, stream=None,
+                   dq_accum: str = "f16") -> Plan:
+    """Device-side plan from q2k int32 [4,T,16] and doc_offsets int32 [D+1].
+    dq_accum: precision of the backward's dQ pool ("f16", "bf16" or "f32")."""
     if q2k.dim() != 3:
         raise ValueError("q2k must be [4, T, 16]")
     T = int(q2k.shape[1])
@@ -167,7 +173,7 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
     nbytes = plan_workspace_bytes(T, D)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q2k.device)
-    opts = MsaPlanOptions(super_block=super_block)
+    opts = MsaPlanOptions(super_block=super_block, dq_accum=DQ_ACCUM[dq_accum])
     st = MsaPlanStruct()
     _check(lib().msa_build_plan(_ptr(q2k), _ptr(doc_offsets), T, D, ctypes.byref(opts),
                                 _ptr(workspace), workspace.numel(), _stream(stream),

@@ -2,17 +2,24 @@
 //
 // Launch sequence as on the pages (NeMo-Automodel PR "feat(minimax-m3) ...",
 // "Custom backward design"): delta preprocess -> zero gradient pools -> main
-// attention backward -> BF16 gradient finalization.  The main kernel is
-// KV-parallel like the pages' design (API page msa_backward_sm100): each CTA
-// walks task rows, keeps the bucket's K/V block resident in shared memory,
-// loads the task's 8 query rows of Q and dO per tile, and per tile issues five
-// 128x128x128 tcgen05 contractions with fp32 accumulators in tensor memory:
-//   S  = Q K^T,   dP = dO V^T,                       (TMEM cols 0 and 128)
-//   dV += P^T dO, dK += dS^T Q  over the bucket run,   (TMEM cols 256, 384)
-//   dQ  = dS K                                         (TMEM cols 0, after S)
-// with P = exp(S * scale - LSE) and dS = P (dP - delta).  dV / dK are flushed
-// with fp32 L2 reductions when the run of tasks on the same block ends; dQ is
-// reduced per tile into an fp32 pool.  The finalize casts the pools to bf16.
+// attention backward -> gradient finalization.  The main kernel is KV-parallel
+// and, like the pages' design (API page msa_backward_sm100), issues its five
+// tcgen05 GEMMs transposed so that the key block is the MMA's M dimension:
+//   S^T  = K Q^T,   dP^T = V dO^T                 (TMEM cols [0,128), [128,256))
+//   P^T  = exp(S^T * scale - LSE),  dS^T = P^T (dP^T - delta)
+//   dV  += P^T dO,  dK += dS^T Q   (A operands read from TMEM; cols 256, 384)
+//   dQ^T = K^T dS^T                 (dS from shared memory; cols [128,256))
+// TMEM lane = key for S/dP/dV/dK, so the per-key softmax work is one thread
+// per key; lane = head dimension for dQ^T, so one warp reduces 32 consecutive
+// dQ elements of a row at a time (coalesced).  dV / dK accumulate over a run
+// of tasks that share the K/V block and are flushed with fp32 L2 reductions;
+// dQ is reduced per tile into an fp16 (default), bf16 or fp32 pool.
+//
+// Warp roles of bwd_main (320 threads):
+//   0      TMA producer: K/V per block run, Q/dO per task (two stages)
+//   1      MMA issuer, TMEM owner
+//   2-5    compute: P^T, dS^T (thread = key)
+//   6-9    reduce:  dQ^T -> pool (thread = head dim), dV / dK flush
 //
 // Kernels, in launch order:
 //   bwd_delta     delta = rowsum(dO * O); zero the dQ / dK / dV pools
@@ -29,12 +36,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdLayout {
   size_t off_delta, off_dq, off_dk, off_dv, total;
 };
+size_t dq_elem_bytes(const msa_plan& p) { return p.dq_accum == MSA_DQ_ACCUM_F32 ? 4 : 2; }
 BwdLayout bwd_layout(const msa_plan& p) {
   BwdLayout L{};
   const int64_t rows = p.T * kQHeads;
   size_t o = 0;
   L.off_delta = o; o = align_up(o + sizeof(float) * rows, 256);
-  L.off_dq = o;    o = align_up(o + sizeof(float) * rows * kHeadDim, 256);
+  L.off_dq = o;    o = align_up(o + dq_elem_bytes(p) * rows * kHeadDim, 256);
   L.off_dk = o;    o = align_up(o + sizeof(float) * p.T * kKVHeads * kHeadDim, 256);
   L.off_dv = o;    o = align_up(o + sizeof(float) * p.T * kKVHeads * kHeadDim, 256);
   L.total = o;
@@ -45,57 +53,82 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ------------------------------------------------------------ bwd_delta
-// One warp per row (t, h): delta = sum_c dO * O (bf16 inputs, fp32 sum), and
-// zero the row of the dQ pool; rows < 4T also zero one row of dK and dV pools.
+// One thread per 8 elements: delta[row] = sum_c dO * O over the row's 128
+// elements (16 threads per row), plus zeroing of the pools.  Each thread
+// handles 4 rows' worth of work so several loads are in flight.
+constexpr int kDeltaRowsPerWarp = 8;
 __global__ void __launch_bounds__(256) k_bwd_delta(msa_plan p, const __nv_bfloat16* O,
                                                    const __nv_bfloat16* dO, float* delta,
-                                                   float* dq_pool, float* dk_pool,
-                                                   float* dv_pool) {
+                                                   uint4* dq_pool, int64_t dq_pool_vec,
+                                                   float4* dkv_pool, int64_t dkv_vec) {
+  if (plan_failed(p.header)) return;
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (row >= p.T * kQHeads || plan_failed(p.header)) return;
-  const uint2 a = reinterpret_cast<const uint2*>(O + row * kHeadDim)[lane];
-  const uint2 b = reinterpret_cast<const uint2*>(dO + row * kHeadDim)[lane];
-  float s = bf16_lo(a.x) * bf16_lo(b.x);
-  s = fmaf(bf16_hi(a.x), bf16_hi(b.x), s);
-  s = fmaf(bf16_lo(a.y), bf16_lo(b.y), s);
-  s = fmaf(bf16_hi(a.y), bf16_hi(b.y), s);
+  const int64_t rows = p.T * kQHeads;
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t r0 = warp0 * kDeltaRowsPerWarp;
+  // lanes 0-15 -> row r, lanes 16-31 -> row r+1 (8 elements each)
+  uint4 a[kDeltaRowsPerWarp / 2], b[kDeltaRowsPerWarp / 2];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) delta[row] = s;
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  reinterpret_cast<float4*>(dq_pool + row * kHeadDim)[lane] = zero;
-  if (row < p.T * kKVHeads) {
-    reinterpret_cast<float4*>(dk_pool + row * kHeadDim)[lane] = zero;
-    reinterpret_cast<float4*>(dv_pool + row * kHeadDim)[lane] = zero;
+  for (int i = 0; i < kDeltaRowsPerWarp / 2; ++i) {
+    const int64_t row = r0 + 2 * i + (lane >> 4);
+    if (row < rows) {
+      a[i] = reinterpret_cast<const uint4*>(O + row * kHeadDim)[lane & 15];
+      b[i] = reinterpret_cast<const uint4*>(dO + row * kHeadDim)[lane & 15];
+    } else {
+      a[i] = b[i] = make_uint4(0, 0, 0, 0);
+    }
   }
+#pragma unroll
+  for (int i = 0; i < kDeltaRowsPerWarp / 2; ++i) {
+    const uint32_t x[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+    const uint32_t y[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s = fmaf(bf16_lo(x[e]), bf16_lo(y[e]), s);
+      s = fmaf(bf16_hi(x[e]), bf16_hi(y[e]), s);
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int64_t row = r0 + 2 * i + (lane >> 4);
+    if ((lane & 15) == 0 && row < rows) delta[row] = s;
+  }
+  // zero the pools with a grid-stride loop of 16-byte stores
+  const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t i = tid; i < dq_pool_vec; i += nthreads) dq_pool[i] = z;
+  const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = tid; i < dkv_vec; i += nthreads) dkv_pool[i] = zf;
 }
 
 // ------------------------------------------------------------ bwd_main
-constexpr int kBwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 compute / reduce
+constexpr int kBwdThreads = 320;
 constexpr uint32_t kTileBytes = 32768;
-constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmDO = 98304, kSmP = 131072,
-                   kSmDS = 163840, kSmStage = 196608;
-constexpr uint32_t kStageFloats = 32 * 33;
-constexpr uint32_t kBwdSmem = kSmStage + 4 * kStageFloats * 4 + 1024;
+constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmDO = 131072, kSmDS = 196608;
+constexpr uint32_t kBwdSmem = kSmDS + kTileBytes + 1024;
 
-constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDV = 256, kTmDK = 384, kTmDQ = 0;
+constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDV = 256, kTmDK = 384;
+constexpr uint32_t kTmP = 0;      // P^T  (bf16 pairs) over S^T,  cols [0,64)
+constexpr uint32_t kTmDST = 128;  // dS^T (bf16 pairs) over dP^T, cols [128,192)
+constexpr uint32_t kTmDQ = 128;   // dQ^T over dP^T, cols [128,256)
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full, qdo_empty, sdp_full, pds_full, dq_full, dq_free, dkv_free,
-      fin;
+  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full, dvdk_done, dq_full,
+      dq_free, dkv_free, fin;
 };
 
 struct BwdParams {
   msa_plan plan;
   const float* lse;
   const float* delta;
-  float* dq_pool;
+  void* dq_pool;
   float* dk_pool;
   float* dv_pool;
   float c2;     // scale * log2(e)
   float scale;
   int chunk;
+  int dq_accum;
 };
 
 __device__ __forceinline__ int64_t cta_task(int64_t i, int chunk) {
@@ -110,30 +143,6 @@ __device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
                                                                     : chunk);
 }
 
-// Reduce 32 rows x 32 fp32 columns held one row per lane (r[]) into global
-// rows dst (one pointer per lane, already offset to the column chunk) with
-// coalesced 16-byte L2 reductions: the warp transposes through `stage`.
-__device__ __forceinline__ void warp_reduce_rows(float* stage, const uint32_t (&r)[32], float mul,
-                                                 float* dst, bool valid) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]) * mul;
-  __syncwarp();
-#pragma unroll
-  for (int rr = 0; rr < 32; rr += 4) {
-    const int src = rr + (lane >> 3);
-    const int c4 = (lane & 7) * 4;
-    float* d = reinterpret_cast<float*>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), src));
-    const bool v = __shfl_sync(0xffffffffu, valid ? 1 : 0, src) != 0;
-    if (v) {
-      const float* s = stage + src * 33 + c4;
-      red_add_v4_f32(d + c4, s[0], s[1], s[2], s[3]);
-    }
-  }
-  __syncwarp();
-}
-
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_main(const __grid_constant__ BwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapK,
@@ -142,6 +151,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ BwdBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
+  __shared__ float s_lse2[128], s_delta[128];
+  __shared__ int32_t s_jlim[128];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -154,10 +165,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     skip_sh = plan_failed(p.header) ? 1 : 0;
     mbar_init(smem_u32(&bars.kv_full), 1);
     mbar_init(smem_u32(&bars.kv_empty), 1);
-    mbar_init(smem_u32(&bars.qdo_full), 1);
-    mbar_init(smem_u32(&bars.qdo_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.qdo_full[i]), 1);
+      mbar_init(smem_u32(&bars.qdo_empty[i]), 1);
+    }
     mbar_init(smem_u32(&bars.sdp_full), 1);
     mbar_init(smem_u32(&bars.pds_full), 128);
+    mbar_init(smem_u32(&bars.dvdk_done), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_free), 128);
     mbar_init(smem_u32(&bars.dkv_free), 128);
@@ -183,11 +197,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&mapDO);
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
-      int prev_sub = -1;
+      int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
       for (; it < my_n; ++it) {
         const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-        if (tv.sub != prev_sub) {
+        if (tv.sub != prev_kv) {
           if (kv_loads > 0 &&
               !mbar_wait(smem_u32(&bars.kv_empty), uint32_t((kv_loads - 1) & 1), abort_flag))
             break;
@@ -198,56 +212,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sbase + kSmV, &mapV, b, 0, tv.g, tv.key_start);
           tma_load_3d(sbase + kSmV + 16384, &mapV, b, 64, tv.g, tv.key_start);
           ++kv_loads;
-          prev_sub = tv.sub;
+          prev_kv = tv.sub;
         }
-        if (it >= 1 && !mbar_wait(smem_u32(&bars.qdo_empty), uint32_t((it - 1) & 1), abort_flag))
+        const int st = int(it & 1);
+        if (it >= 2 &&
+            !mbar_wait(smem_u32(&bars.qdo_empty[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
           break;
-        const uint32_t b = smem_u32(&bars.qdo_full);
+        const uint32_t b = smem_u32(&bars.qdo_full[st]);
         mbar_arrive_expect_tx(b, 2 * kTileBytes);
+        const uint32_t dq = sbase + kSmQ + st * kTileBytes, dd = sbase + kSmDO + st * kTileBytes;
         for (int qi = 0; qi < kTaskQueries; ++qi) {
           const int32_t tok = p.col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
           const int y = tok * kQHeads + tv.g * kHeadsPerGroup;
-          tma_load_2d(sbase + kSmQ + qi * 2048, &mapQ, b, 0, y);
-          tma_load_2d(sbase + kSmQ + 16384 + qi * 2048, &mapQ, b, 64, y);
-          tma_load_2d(sbase + kSmDO + qi * 2048, &mapDO, b, 0, y);
-          tma_load_2d(sbase + kSmDO + 16384 + qi * 2048, &mapDO, b, 64, y);
+          tma_load_2d(dq + qi * 2048, &mapQ, b, 0, y);
+          tma_load_2d(dq + 16384 + qi * 2048, &mapQ, b, 64, y);
+          tma_load_2d(dd + qi * 2048, &mapDO, b, 0, y);
+          tma_load_2d(dd + 16384 + qi * 2048, &mapDO, b, 64, y);
         }
       }
       if (*abort_flag) {  // let armed copies land before the CTA exits
         if (kv_loads > 0) mbar_wait_drain(smem_u32(&bars.kv_full), uint32_t((kv_loads - 1) & 1));
-        if (it > 0) mbar_wait_drain(smem_u32(&bars.qdo_full), uint32_t((it - 1) & 1));
+        for (int64_t j = (it >= 2 ? it - 2 : 0); j < it; ++j)
+          mbar_wait_drain(smem_u32(&bars.qdo_full[j & 1]), uint32_t((j >> 1) & 1));
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && my_n > 0) {
-      constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S, dP
-      constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dV, dK
-      constexpr uint32_t idKM = idesc_bf16_f32(128, 128, 0, 1);  // dQ
-      int cur_sub = -1;
+      constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t idTS = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
+      constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T
       int64_t kv_loads = 0, seg_done = 0;
       bool first_in_seg = true;
-      for (int64_t it = 0; it < my_n; ++it) {
-        const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-        if (tv.sub != cur_sub) {
-          if (it > 0) umma_commit(smem_u32(&bars.kv_empty));
-          if (!mbar_wait(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) break;
-          ++kv_loads;
-          cur_sub = tv.sub;
-          first_in_seg = true;
-        }
-        if (!mbar_wait(smem_u32(&bars.qdo_full), uint32_t(it & 1), abort_flag)) break;
+      auto issue_S = [&](int64_t it) -> bool {
+        const int st = int(it & 1);
+        if (!mbar_wait(smem_u32(&bars.qdo_full[st]), uint32_t((it >> 1) & 1), abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t sq = sbase + kSmQ + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + kTmS, desc_kmajor(sbase + kSmK, kk), desc_kmajor(sq, kk), idKK, kk > 0);
+        return true;
+      };
+      int cur_kv = decode_task(tasks[cta_task(0, prm.chunk)]).sub;
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort_flag);
+      kv_loads = 1;
+      ok = ok && issue_S(0);
+      for (int64_t it = 0; ok && it < my_n; ++it) {
+        const int st = int(it & 1);
+        // dP^T(it) overwrites dQ^T(it-1): the reducers must have read it.
         if (it >= 1 && !mbar_wait(smem_u32(&bars.dq_free), uint32_t((it - 1) & 1), abort_flag))
           break;
         tc_fence_after();
+        const uint32_t sdo = sbase + kSmDO + st * kTileBytes;
+        const uint32_t sq = sbase + kSmQ + st * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmS, desc_kmajor(sbase + kSmQ, kk), desc_kmajor(sbase + kSmK, kk), idKK,
+          umma_ss(tmem + kTmDP, desc_kmajor(sbase + kSmV, kk), desc_kmajor(sdo, kk), idKK,
                   kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDP, desc_kmajor(sbase + kSmDO, kk), desc_kmajor(sbase + kSmV, kk),
-                  idKK, kk > 0);
         umma_commit(smem_u32(&bars.sdp_full));
         if (!mbar_wait(smem_u32(&bars.pds_full), uint32_t(it & 1), abort_flag)) break;
         if (first_in_seg && seg_done > 0 &&
@@ -257,106 +280,185 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t acc0 = first_in_seg ? 0u : 1u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDV, desc_mnmajor(sbase + kSmP, kk), desc_mnmajor(sbase + kSmDO, kk),
-                  idMM, kk > 0 ? 1u : acc0);
+          umma_ts(tmem + kTmDV, tmem + kTmP + kk * 8, desc_mnmajor(sdo, kk), idTS,
+                  kk > 0 ? 1u : acc0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDK, desc_mnmajor(sbase + kSmDS, kk), desc_mnmajor(sbase + kSmQ, kk),
-                  idMM, kk > 0 ? 1u : acc0);
+          umma_ts(tmem + kTmDK, tmem + kTmDST + kk * 8, desc_mnmajor(sq, kk), idTS,
+                  kk > 0 ? 1u : acc0);
+        umma_commit(smem_u32(&bars.dvdk_done));
+        // dQ^T is written over dS^T / dP^T: wait until dK has read dS^T.
+        if (!mbar_wait(smem_u32(&bars.dvdk_done), uint32_t(it & 1), abort_flag)) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDQ, desc_kmajor(sbase + kSmDS, kk), desc_mnmajor(sbase + kSmK, kk),
-                  idKM, kk > 0);
+          umma_ss(tmem + kTmDQ, desc_mnmajor(sbase + kSmK, kk), desc_mnmajor(sbase + kSmDS, kk),
+                  idMM, kk > 0);
         umma_commit(smem_u32(&bars.dq_full));
-        umma_commit(smem_u32(&bars.qdo_empty));
+        umma_commit(smem_u32(&bars.qdo_empty[st]));
         first_in_seg = false;
-        const bool seg_end =
-            (it + 1 == my_n) || decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub != cur_sub;
-        if (seg_end) ++seg_done;
+        if (it + 1 < my_n) {
+          const int next_kv = decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub;
+          if (next_kv != cur_kv) {
+            ++seg_done;
+            umma_commit(smem_u32(&bars.kv_empty));
+            if (!mbar_wait(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) break;
+            ++kv_loads;
+            cur_kv = next_kv;
+            first_in_seg = true;
+          }
+          // S^T(it+1) overwrites P^T(it): dV(it) is complete (dvdk_done).
+          if (!issue_S(it + 1)) break;
+        }
       }
       umma_commit(smem_u32(&bars.fin));
       mbar_wait_drain(smem_u32(&bars.fin), 0);
     }
-  } else {
-    // ---------------- compute: softmax / dS, dQ reduction, dK / dV flush
+  } else if (warp < 6) {
+    // ---------------- compute: P^T, dS^T (thread = key)
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;
+    const int r = quad * 32 + lane;  // key within the block = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    float* stage = reinterpret_cast<float*>(smem + kSmStage) + (warp - 2) * kStageFloats;
     for (int64_t it = 0; it < my_n; ++it) {
       const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-      const int qi = row >> 4, hh = row & 15;
-      const bool row_valid = qi < tv.nq;
-      const int32_t tok = p.col[tv.col_begin + (row_valid ? qi : tv.nq - 1)];
-      const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      int jmax = tok - tv.key_start;
-      if (jmax > tv.key_len - 1) jmax = tv.key_len - 1;
-      if (!row_valid) jmax = -1;
-      const float lse2 = prm.lse[grow] * kLog2e;
-      const float dl = prm.delta[grow];
+      // per-column scalars: thread r fills column r (q-row r = 16 qi + hh)
+      {
+        const int qi = r >> 4, hh = r & 15;
+        const bool valid = qi < tv.nq;
+        const int32_t tok = p.col[tv.col_begin + (valid ? qi : tv.nq - 1)];
+        const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
+        int jl = tok - tv.key_start;
+        if (jl > tv.key_len - 1) jl = tv.key_len - 1;
+        const float l2 = prm.lse[grow] * kLog2e;
+        const float dl = prm.delta[grow];
+        named_bar_sync(1, 128);  // previous task's columns fully consumed
+        s_lse2[r] = l2;
+        s_delta[r] = dl;
+        s_jlim[r] = valid ? jl : -1;
+        named_bar_sync(1, 128);
+      }
       if (!mbar_wait_warp(smem_u32(&bars.sdp_full), uint32_t(it & 1), abort_flag)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tmem + lane_base + kTmS + c * 32, s);
-        tmem_ld32(tmem + lane_base + kTmDP + c * 32, dp);
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_base + kTmS + c * 32, sv);
+        tmem_ld32(tmem + lane_base + kTmDP + c * 32, dv);
         tmem_ld_wait();
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const int k0 = c * 32 + j;
-          const float p0 = (k0 <= jmax) ? fast_exp2(fmaf(__uint_as_float(s[j]), prm.c2, -lse2)) : 0.f;
+          const int col = c * 32 + j;
+          const float p0 = (r <= s_jlim[col])
+                               ? fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -s_lse2[col]))
+                               : 0.f;
           const float p1 =
-              (k0 + 1 <= jmax) ? fast_exp2(fmaf(__uint_as_float(s[j + 1]), prm.c2, -lse2)) : 0.f;
-          const float d0 = p0 * (__uint_as_float(dp[j]) - dl);
-          const float d1 = p1 * (__uint_as_float(dp[j + 1]) - dl);
+              (r <= s_jlim[col + 1])
+                  ? fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -s_lse2[col + 1]))
+                  : 0.f;
+          const float d0 = p0 * (__uint_as_float(dv[j]) - s_delta[col]);
+          const float d1 = p1 * (__uint_as_float(dv[j + 1]) - s_delta[col + 1]);
           pp[j >> 1] = pack_bf16x2(p0, p1);
           pd[j >> 1] = pack_bf16x2(d0, d1);
         }
-        const uint32_t off = (c >> 1) * 16384 + row * 128;
+        // P^T over S^T cols [16c, 16c+16), dS^T over dP^T cols [128+16c, ...):
+        // both only cover columns this thread has already read.
+        tmem_st16(tmem + lane_base + kTmP + c * 16, pp);
+        tmem_st16(tmem + lane_base + kTmDST + c * 16, pd);
+        // dS (B operand of dQ^T, MN-major): tile row = key r, cols = q-rows
+        const uint32_t rowb = sbase + kSmDS + (c >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t ch = (((c & 1) * 4 + u) ^ (row & 7)) * 16;
-          st_shared_v4(sbase + kSmP + off + ch, pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-          st_shared_v4(sbase + kSmDS + off + ch, pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+          const uint32_t ch = (((c & 1) * 4 + u) ^ (r & 7)) * 16;
+          st_shared_v4(rowb + ch, pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
         }
       }
+      tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.pds_full));
-
-      // dQ: reduce scale * (dS K) rows into the pool
+    }
+  } else {
+    // ---------------- reduce: dQ^T -> pool (thread = head dim), dV / dK flush
+    const int quad = warp & 3;
+    const int d = quad * 32 + lane;  // head dim = TMEM lane (dQ^T); key for dV / dK
+    const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    for (int64_t it = 0; it < my_n; ++it) {
+      const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
+      int32_t tok[kTaskQueries];
+#pragma unroll
+      for (int qi = 0; qi < kTaskQueries; ++qi)
+        tok[qi] = p.col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
       if (!mbar_wait_warp(smem_u32(&bars.dq_full), uint32_t(it & 1), abort_flag)) break;
       tc_fence_after();
-      float* dq_row = prm.dq_pool + grow * kHeadDim;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kTmDQ + c * 32, r);
-        tmem_ld_wait();
-        warp_reduce_rows(stage, r, prm.scale, dq_row + c * 32, row_valid);
-      }
+      uint32_t v[128];
+      tmem_ld32(tmem + lane_base + kTmDQ + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem + lane_base + kTmDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(tmem + lane_base + kTmDQ + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+      tmem_ld32(tmem + lane_base + kTmDQ + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.dq_free));
-
-      // end of a run of tasks on this K/V block: flush dV and dK (lane = key)
+      const int64_t gbase = int64_t(tv.g) * kHeadsPerGroup;
+      if (prm.dq_accum == MSA_DQ_ACCUM_F32) {
+        float* pool = static_cast<float*>(prm.dq_pool);
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const int qi = j >> 4;
+          if (qi < tv.nq) {
+            const int64_t row = int64_t(tok[qi]) * kQHeads + gbase + (j & 15);
+            red_add_f32(pool + row * kHeadDim + d, __uint_as_float(v[j]) * prm.scale);
+          }
+        }
+      } else {
+        // even lanes reduce (row j, dims d, d+1), odd lanes (row j+1, dims d-1, d)
+        const bool odd = lane & 1;
+        uint16_t* pool = static_cast<uint16_t*>(prm.dq_pool);
+        const bool f16 = prm.dq_accum == MSA_DQ_ACCUM_F16;
+#pragma unroll
+        for (int j = 0; j < 128; j += 2) {
+          const float a = __uint_as_float(v[j]) * prm.scale;
+          const float b = __uint_as_float(v[j + 1]) * prm.scale;
+          const float x = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+          const int jr = odd ? j + 1 : j;
+          const int qi = jr >> 4;
+          if (qi < tv.nq) {
+            const int64_t row = int64_t(tok[qi]) * kQHeads + gbase + (jr & 15);
+            uint16_t* dst = pool + row * kHeadDim + (odd ? d - 1 : d);
+            const float lo = odd ? x : a, hi = odd ? b : x;
+            if (f16)
+              red_add_f16x2(dst, pack_f16x2(lo, hi));
+            else
+              red_add_bf16x2(dst, pack_bf16x2(lo, hi));
+          }
+        }
+      }
       const bool seg_end =
           (it + 1 == my_n) || decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub != tv.sub;
       if (seg_end) {
-        const bool key_valid = row < tv.key_len;
-        const int64_t krow = (int64_t(tv.key_start) + row) * kKVHeads + tv.g;
-        float* dv_row = prm.dv_pool + krow * kHeadDim;
-        float* dk_row = prm.dk_pool + krow * kHeadDim;
+        // dq_full(it) follows dvdk_done(it): dV / dK of the run are final.
+        const int key = d;
+        const bool key_valid = key < tv.key_len;
+        const int64_t krow = (int64_t(tv.key_start) + key) * kKVHeads + tv.g;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kTmDV + c * 32, r);
+          uint32_t a[32], b[32];
+          tmem_ld32(tmem + lane_base + kTmDV + c * 32, a);
+          tmem_ld32(tmem + lane_base + kTmDK + c * 32, b);
           tmem_ld_wait();
-          warp_reduce_rows(stage, r, 1.f, dv_row + c * 32, key_valid);
-          tmem_ld32(tmem + lane_base + kTmDK + c * 32, r);
-          tmem_ld_wait();
-          warp_reduce_rows(stage, r, prm.scale, dk_row + c * 32, key_valid);
+          if (key_valid) {
+            float* dvr = prm.dv_pool + krow * kHeadDim + c * 32;
+            float* dkr = prm.dk_pool + krow * kHeadDim + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              red_add_v4_f32(dvr + e, __uint_as_float(a[e]), __uint_as_float(a[e + 1]),
+                             __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+              red_add_v4_f32(dkr + e, __uint_as_float(b[e]) * prm.scale,
+                             __uint_as_float(b[e + 1]) * prm.scale,
+                             __uint_as_float(b[e + 2]) * prm.scale,
+                             __uint_as_float(b[e + 3]) * prm.scale);
+            }
+          }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dkv_free));
@@ -371,29 +473,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------ bwd_finalize
-// fp32 pools -> bf16 outputs; one warp per 128-element row.
-__global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const float* dq_pool,
+// Pools -> bf16 outputs, 8 elements per thread.
+__global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq_pool,
                                                       const float* dk_pool, const float* dv_pool,
                                                       __nv_bfloat16* dq, __nv_bfloat16* dk,
                                                       __nv_bfloat16* dv) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nq = p.T * kQHeads, nk = p.T * kKVHeads;
-  if (row >= nq + 2 * nk || plan_failed(p.header)) return;
-  const float* src;
-  __nv_bfloat16* dst;
-  if (row < nq) {
-    src = dq_pool + row * kHeadDim;
-    dst = dq + row * kHeadDim;
-  } else if (row < nq + nk) {
-    src = dk_pool + (row - nq) * kHeadDim;
-    dst = dk + (row - nq) * kHeadDim;
-  } else {
-    src = dv_pool + (row - nq - nk) * kHeadDim;
-    dst = dv + (row - nq - nk) * kHeadDim;
+  if (plan_failed(p.header)) return;
+  const int64_t nq8 = p.T * kQHeads * kHeadDim / 8, nk8 = p.T * kKVHeads * kHeadDim / 8;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq8 + 2 * nk8;
+       i += stride) {
+    float f[8];
+    uint4* dst;
+    if (i < nq8) {
+      if (p.dq_accum == MSA_DQ_ACCUM_F32) {
+        const float4 a = reinterpret_cast<const float4*>(dq_pool)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(dq_pool)[2 * i + 1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      } else {
+        const uint4 a = reinterpret_cast<const uint4*>(dq_pool)[i];
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (p.dq_accum == MSA_DQ_ACCUM_F16) {
+            f[2 * e] = f16_lo(w[e]);
+            f[2 * e + 1] = f16_hi(w[e]);
+          } else {
+            f[2 * e] = bf16_lo(w[e]);
+            f[2 * e + 1] = bf16_hi(w[e]);
+          }
+        }
+      }
+      dst = reinterpret_cast<uint4*>(dq) + i;
+    } else {
+      const int64_t j = i < nq8 + nk8 ? i - nq8 : i - nq8 - nk8;
+      const float* src = i < nq8 + nk8 ? dk_pool : dv_pool;
+      const float4 a = reinterpret_cast<const float4*>(src)[2 * j];
+      const float4 b = reinterpret_cast<const float4*>(src)[2 * j + 1];
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+      f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      dst = reinterpret_cast<uint4*>(i < nq8 + nk8 ? dk : dv) + j;
+    }
+    *dst = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
   }
-  const float4 x = reinterpret_cast<const float4*>(src)[lane];
-  reinterpret_cast<uint2*>(dst)[lane] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
 }
 
 }  // namespace
@@ -410,7 +534,7 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   const BwdLayout L = bwd_layout(p);
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* delta = reinterpret_cast<float*>(w + L.off_delta);
-  float* dq_pool = reinterpret_cast<float*>(w + L.off_dq);
+  void* dq_pool = w + L.off_dq;
   float* dk_pool = reinterpret_cast<float*>(w + L.off_dk);
   float* dv_pool = reinterpret_cast<float*>(w + L.off_dv);
 
@@ -421,10 +545,14 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
     return cudaErrorInvalidValue;
 
   const int64_t rows = p.T * kQHeads;
+  const int64_t dq_vec = int64_t(dq_elem_bytes(p)) * rows * kHeadDim / 16;
+  // dk and dv pools are contiguous in the workspace (dv follows dk)
+  const int64_t dkv_vec = int64_t(L.off_dv - L.off_dk) / 16 + p.T * kKVHeads * kHeadDim / 4;
+  const int64_t warps = (rows + kDeltaRowsPerWarp - 1) / kDeltaRowsPerWarp;
   launch_begin("bwd_delta", s);
-  k_bwd_delta<<<unsigned((rows + 7) / 8), 256, 0, s>>>(
+  k_bwd_delta<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
       p, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
-      dq_pool, dk_pool, dv_pool);
+      static_cast<uint4*>(dq_pool), dq_vec, reinterpret_cast<float4*>(dk_pool), dkv_vec);
   launch_end("bwd_delta", s);
 
   static bool attr_set = false;
@@ -434,13 +562,13 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 8};
+  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 16,
+                p.dq_accum};
   launch_begin("bwd_main", s);
   k_bwd_main<<<unsigned(device_sm_count()), kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
   launch_end("bwd_main", s);
-  const int64_t frows = rows + 2 * p.T * kKVHeads;
   launch_begin("bwd_finalize", s);
-  k_bwd_finalize<<<unsigned((frows + 7) / 8), 256, 0, s>>>(
+  k_bwd_finalize<<<unsigned(device_sm_count() * 8), 256, 0, s>>>(
       p, dq_pool, dk_pool, dv_pool, static_cast<__nv_bfloat16*>(dq),
       static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
   launch_end("bwd_finalize", s);

@@ -198,7 +198,8 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   if (!q2k || !doc_offsets || !workspace || !out) return MSA_ERR_INVALID_ARG;
   if (T < 1 || T > kMaxTokens || num_docs < 1 || num_docs > T) return MSA_ERR_INVALID_ARG;
   const int32_t Z = opts ? opts->super_block : 16;
-  if (Z < 0) return MSA_ERR_INVALID_ARG;
+  const int32_t acc = opts ? opts->dq_accum : MSA_DQ_ACCUM_F16;
+  if (Z < 0 || acc < MSA_DQ_ACCUM_F16 || acc > MSA_DQ_ACCUM_F32) return MSA_ERR_INVALID_ARG;
   if (!aligned16(q2k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(doc_offsets) & 3u))
     return MSA_ERR_ALIGNMENT;
   const PlanLayout L = plan_layout(T, num_docs);
@@ -210,6 +211,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   p.T = T;
   p.num_docs = num_docs;
   p.super_block = Z;
+  p.dq_accum = acc;
   p.nb_cap = L.nb_cap;
   p.tri_cap = L.tri_cap;
   p.nnz_cap = L.nnz_cap;

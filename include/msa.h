@@ -69,12 +69,23 @@ typedef enum msa_status {
 /* Human-readable name of a status code (static string). */
 const char* msa_status_string(msa_status s);
 
+/* Precision of the dQ accumulation pool of msa_backward.  The pages' default
+ * is packed FP16 atomics with a BF16 switch for range ("Supported scope":
+ * MSA_M3_DQ_ACCUM); FP32 is the widest and slowest. */
+typedef enum msa_dq_accum {
+  MSA_DQ_ACCUM_F16 = 0,
+  MSA_DQ_ACCUM_BF16 = 1,
+  MSA_DQ_ACCUM_F32 = 2
+} msa_dq_accum;
+
 /* Plan-build options.  Pass NULL for the defaults. */
 typedef struct msa_plan_options {
   /* Tasks of one (index head, key block) bucket are cut at runs of
    * super_block consecutive query blocks (0 = never cut).  Default 16. */
   int32_t super_block;
-  int32_t reserved[7];
+  /* An msa_dq_accum value.  Default MSA_DQ_ACCUM_F16. */
+  int32_t dq_accum;
+  int32_t reserved[6];
 } msa_plan_options;
 
 /*
@@ -96,6 +107,8 @@ typedef struct msa_plan {
   int64_t T;
   int32_t num_docs;
   int32_t super_block;
+  int32_t dq_accum;
+  int32_t reserved0;
   int64_t nb_cap;     /* bound on the number of 128-key blocks            */
   int64_t tri_cap;    /* bound on (index head, doc, key block, query block) */
   int64_t nnz_cap;    /* bound on CSR entries                              */

@@ -56,9 +56,10 @@ def oracle_results(name):
     return w, O, L, dQ, dK, dV
 
 
-def run_gpu(w, super_block=16):
+def run_gpu(w, super_block=16, dq_accum="f16"):
     q, k, v, do = (x.to(DEV) for x in (w.q, w.k, w.v, w.do))
-    plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=super_block)
+    plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=super_block,
+                              dq_accum=dq_accum)
     o, lse = api.msa_forward(plan, q, k, v, w.scale)
     dq, dk, dv = api.msa_backward(plan, q, k, v, o, lse, do, w.scale)
     torch.cuda.synchronize()
@@ -89,6 +90,15 @@ def test_super_block_lengths_agree(Z):
     o, lse, dq, dk, dv = run_gpu(w, super_block=Z)
     check_o(o, O)
     check_lse(lse, L)
+    check_grad(dq, dQ, "dQ")
+    check_grad(dk, dK, "dK")
+    check_grad(dv, dV, "dV")
+
+
+@pytest.mark.parametrize("acc", ["f32", "bf16"])
+def test_dq_pool_precisions(acc):
+    w, O, L, dQ, dK, dV = oracle_results("multidoc-ragged")
+    _, _, dq, dk, dv = run_gpu(w, dq_accum=acc)
     check_grad(dq, dQ, "dQ")
     check_grad(dk, dK, "dK")
     check_grad(dv, dV, "dV")
