@@ -274,15 +274,17 @@ def run_gpu(args, rank, world):
         hdk.copy_(dk, non_blocking=True)
         hdv.copy_(dv, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ea.record(stream)
-    for _ in range(e2e_steps):
+    e2e_ms = float("nan")
+    if not args.no_e2e:
         e2e_step()
-    eb.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = ea.elapsed_time(eb) / e2e_steps
     if world > 1:
         t = torch.tensor([e2e_ms], dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -345,6 +347,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--super-block", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
