@@ -15,11 +15,9 @@
 // of tasks that share the K/V block and are flushed with fp32 L2 reductions;
 // dQ is reduced per tile into an fp16 (default), bf16 or fp32 pool.
 //
-// Warp roles of bwd_main (320 threads):
-//   0      TMA producer: K/V per block run, Q/dO per task (two stages)
-//   1      MMA issuer, TMEM owner
-//   2-5    compute: P^T, dS^T (thread = key)
-//   6-9    reduce:  dQ^T -> pool (thread = head dim), dV / dK flush
+// bwd_main runs 14 warps: a TMA producer, an MMA issuer, eight compute warps
+// (P^T, dS^T; two per TMEM lane quadrant, each owning 64 q-rows) and four
+// reduce warps (dQ^T staging + bulk tensor reduction, dV / dK flush).
 //
 // Kernels, in launch order:
 //   bwd_delta     delta = rowsum(dO * O); zero the dQ / dK / dV pools
@@ -27,6 +25,8 @@
 //   bwd_finalize  pools -> bf16 dQ, dK, dV
 #include "common.cuh"
 #include "sm100.cuh"
+
+#include <cstring>
 
 namespace msa {
 namespace {
@@ -103,19 +103,22 @@ __global__ void __launch_bounds__(256) k_bwd_delta(msa_plan p, const __nv_bfloat
 }
 
 // ------------------------------------------------------------ bwd_main
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
 constexpr uint32_t kTileBytes = 32768;
 constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmDO = 131072, kSmDS = 196608;
 constexpr uint32_t kBwdSmem = kSmDS + kTileBytes + 1024;
 
+// TMEM columns.  P^T of q-rows [64h, 64h+64) is packed into S^T columns
+// [64h, 64h+32) and dS^T into dP^T columns [128+64h, 128+64h+32), so each
+// compute half only overwrites S^T / dP^T columns it has already read.
 constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDV = 256, kTmDK = 384;
-constexpr uint32_t kTmP = 0;      // P^T  (bf16 pairs) over S^T,  cols [0,64)
-constexpr uint32_t kTmDST = 128;  // dS^T (bf16 pairs) over dP^T, cols [128,192)
-constexpr uint32_t kTmDQ = 128;   // dQ^T over dP^T, cols [128,256)
+constexpr uint32_t kTmP = 0, kTmDST = 128, kTmDQ = 128;
+// A-operand column of k-step kk (q-rows 16kk..16kk+15) for P^T / dS^T.
+__device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full, dvdk_done, dq_full,
-      dq_free, dkv_free, fin;
+  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full, dk_done, dv_done,
+      dq_full, dq_free, dkv_free, fin;
 };
 
 struct BwdParams {
@@ -142,17 +145,32 @@ __device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
   return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
                                                                     : chunk);
 }
+// Task record i of this CTA's walk, or an empty record past the end.
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n, int chunk) {
+  return i < n ? tasks[cta_task(i, chunk)] : make_int4(0, 0, 1 << 8, -1);
+}
+__device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
+  return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
+}
 
+// Warp roles (448 threads):
+//   0      TMA producer: K/V per block run, Q/dO per task (two stages)
+//   1      MMA issuer, TMEM owner
+//   2-9    compute: P^T, dS^T; warps 2-5 own q-rows [0,64), warps 6-9 [64,128)
+//   10-13  reduce: dQ^T -> pool (thread = head dim), dV / dK flush
+template <int ACC>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_main(const __grid_constant__ BwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapK,
-               const __grid_constant__ CUtensorMap mapV) {
+               const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDQ) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
-  __shared__ float s_lse2[128], s_delta[128];
-  __shared__ int32_t s_jlim[128];
+  __shared__ __align__(16) float s_lse2[128];
+  __shared__ __align__(16) float s_delta[128];
+  __shared__ __align__(16) int8_t s_jlim[128];
+  __shared__ int s_wfull[4];  // per lane quadrant: every column sees all 128 keys
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -170,8 +188,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bars.qdo_empty[i]), 1);
     }
     mbar_init(smem_u32(&bars.sdp_full), 1);
-    mbar_init(smem_u32(&bars.pds_full), 128);
-    mbar_init(smem_u32(&bars.dvdk_done), 1);
+    mbar_init(smem_u32(&bars.pds_full), 256);
+    mbar_init(smem_u32(&bars.dk_done), 1);
+    mbar_init(smem_u32(&bars.dv_done), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_free), 128);
     mbar_init(smem_u32(&bars.dkv_free), 128);
@@ -189,9 +208,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
   const int64_t my_n = cta_task_count(ntasks, prm.chunk);
   const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
+  const int chunk = prm.chunk;
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (task records and tokens prefetched one task ahead)
     if (lane == 0 && my_n > 0) {
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapDO);
@@ -199,8 +219,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
+      int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+      int32_t tok[kTaskQueries];
+      {
+        const TaskView tv = decode_task(rec);
+#pragma unroll
+        for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = task_token(p.col, tv, qi);
+      }
       for (; it < my_n; ++it) {
-        const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
+        const TaskView tv = decode_task(rec);
+        const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+        int32_t tok1[kTaskQueries];
+        {
+          const TaskView tv1 = decode_task(rec1);
+#pragma unroll
+          for (int qi = 0; qi < kTaskQueries; ++qi)
+            tok1[qi] = it + 1 < my_n ? task_token(p.col, tv1, qi) : 0;
+        }
         if (tv.sub != prev_kv) {
           if (kv_loads > 0 &&
               !mbar_wait(smem_u32(&bars.kv_empty), uint32_t((kv_loads - 1) & 1), abort_flag))
@@ -221,14 +256,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t b = smem_u32(&bars.qdo_full[st]);
         mbar_arrive_expect_tx(b, 2 * kTileBytes);
         const uint32_t dq = sbase + kSmQ + st * kTileBytes, dd = sbase + kSmDO + st * kTileBytes;
+#pragma unroll
         for (int qi = 0; qi < kTaskQueries; ++qi) {
-          const int32_t tok = p.col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
-          const int y = tok * kQHeads + tv.g * kHeadsPerGroup;
+          const int y = tok[qi] * kQHeads + tv.g * kHeadsPerGroup;
           tma_load_2d(dq + qi * 2048, &mapQ, b, 0, y);
           tma_load_2d(dq + 16384 + qi * 2048, &mapQ, b, 64, y);
           tma_load_2d(dd + qi * 2048, &mapDO, b, 0, y);
           tma_load_2d(dd + 16384 + qi * 2048, &mapDO, b, 64, y);
         }
+        rec = rec1;
+        rec1 = rec2;
+#pragma unroll
+        for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = tok1[qi];
       }
       if (*abort_flag) {  // let armed copies land before the CTA exits
         if (kv_loads > 0) mbar_wait_drain(smem_u32(&bars.kv_full), uint32_t((kv_loads - 1) & 1));
@@ -255,12 +294,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tmem + kTmS, desc_kmajor(sbase + kSmK, kk), desc_kmajor(sq, kk), idKK, kk > 0);
         return true;
       };
-      int cur_kv = decode_task(tasks[cta_task(0, prm.chunk)]).sub;
+      int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
+      int next_kv = task_rec(tasks, 1, my_n, chunk).w;
       bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort_flag);
       kv_loads = 1;
       ok = ok && issue_S(0);
       for (int64_t it = 0; ok && it < my_n; ++it) {
         const int st = int(it & 1);
+        const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;  // used next iteration
         // dP^T(it) overwrites dQ^T(it-1): the reducers must have read it.
         if (it >= 1 && !mbar_wait(smem_u32(&bars.dq_free), uint32_t((it - 1) & 1), abort_flag))
           break;
@@ -280,25 +321,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t acc0 = first_in_seg ? 0u : 1u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kTmDV, tmem + kTmP + kk * 8, desc_mnmajor(sdo, kk), idTS,
+          umma_ts(tmem + kTmDK, tmem + kTmDST + ts_col(kk), desc_mnmajor(sq, kk), idTS,
                   kk > 0 ? 1u : acc0);
+        umma_commit(smem_u32(&bars.dk_done));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kTmDK, tmem + kTmDST + kk * 8, desc_mnmajor(sq, kk), idTS,
+          umma_ts(tmem + kTmDV, tmem + kTmP + ts_col(kk), desc_mnmajor(sdo, kk), idTS,
                   kk > 0 ? 1u : acc0);
-        umma_commit(smem_u32(&bars.dvdk_done));
-        // dQ^T is written over dS^T / dP^T: wait until dK has read dS^T.
-        if (!mbar_wait(smem_u32(&bars.dvdk_done), uint32_t(it & 1), abort_flag)) break;
+        umma_commit(smem_u32(&bars.dv_done));
+        // dQ^T is written over dS^T: dK must have read it (dV keeps the pipe busy).
+        if (!mbar_wait(smem_u32(&bars.dk_done), uint32_t(it & 1), abort_flag)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + kTmDQ, desc_mnmajor(sbase + kSmK, kk), desc_mnmajor(sbase + kSmDS, kk),
                   idMM, kk > 0);
         umma_commit(smem_u32(&bars.dq_full));
-        umma_commit(smem_u32(&bars.qdo_empty[st]));
         first_in_seg = false;
         if (it + 1 < my_n) {
-          const int next_kv = decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub;
           if (next_kv != cur_kv) {
             ++seg_done;
             umma_commit(smem_u32(&bars.kv_empty));
@@ -307,136 +347,205 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             cur_kv = next_kv;
             first_in_seg = true;
           }
-          // S^T(it+1) overwrites P^T(it): dV(it) is complete (dvdk_done).
+          // S^T(it+1) overwrites P^T(it): dV(it) must have read it (dQ^T keeps the pipe busy).
+          if (!mbar_wait(smem_u32(&bars.dv_done), uint32_t(it & 1), abort_flag)) break;
           if (!issue_S(it + 1)) break;
         }
+        next_kv = next2_kv;
       }
       umma_commit(smem_u32(&bars.fin));
       mbar_wait_drain(smem_u32(&bars.fin), 0);
     }
-  } else if (warp < 6) {
-    // ---------------- compute: P^T, dS^T (thread = key)
+  } else if (warp < 10) {
+    // ---------------- compute: P^T, dS^T (thread = key; half = block of 64 q-rows)
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // key within the block = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    for (int64_t it = 0; it < my_n; ++it) {
-      const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-      // per-column scalars: thread r fills column r (q-row r = 16 qi + hh)
-      {
-        const int qi = r >> 4, hh = r & 15;
-        const bool valid = qi < tv.nq;
-        const int32_t tok = p.col[tv.col_begin + (valid ? qi : tv.nq - 1)];
-        const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-        int jl = tok - tv.key_start;
-        if (jl > tv.key_len - 1) jl = tv.key_len - 1;
-        const float l2 = prm.lse[grow] * kLog2e;
-        const float dl = prm.delta[grow];
-        named_bar_sync(1, 128);  // previous task's columns fully consumed
-        s_lse2[r] = l2;
-        s_delta[r] = dl;
-        s_jlim[r] = valid ? jl : -1;
-        named_bar_sync(1, 128);
+    // One 16-column sub-chunk (q-rows cb .. cb+15, cb = 64 half + 16 sc).
+    auto sub_chunk = [&](int sc, const uint32_t (&sv)[16], const uint32_t (&dv)[16], bool full) {
+      const int cb = half * 64 + sc * 16;
+      const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + cb);
+      const float4* d4 = reinterpret_cast<const float4*>(s_delta + cb);
+      const uint4 jw = *reinterpret_cast<const uint4*>(s_jlim + cb);
+      const uint32_t jwa[4] = {jw.x, jw.y, jw.z, jw.w};
+      float lse[16], dl[16];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 x = l4[q4], y = d4[q4];
+        lse[4 * q4] = x.x; lse[4 * q4 + 1] = x.y; lse[4 * q4 + 2] = x.z; lse[4 * q4 + 3] = x.w;
+        dl[4 * q4] = y.x; dl[4 * q4 + 1] = y.y; dl[4 * q4 + 2] = y.z; dl[4 * q4 + 3] = y.w;
       }
+      uint32_t pp[8], pd[8];
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -lse[j]));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -lse[j + 1]));
+          pp[j >> 1] = pack_bf16x2(p0, p1);
+          pd[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[j]) - dl[j]),
+                                   p1 * (__uint_as_float(dv[j + 1]) - dl[j + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const int jl0 = int(int8_t((jwa[j >> 2] >> (8 * (j & 3))) & 0xFF));
+          const int jl1 = int(int8_t((jwa[j >> 2] >> (8 * ((j + 1) & 3))) & 0xFF));
+          const float p0 =
+              r <= jl0 ? fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -lse[j])) : 0.f;
+          const float p1 =
+              r <= jl1 ? fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -lse[j + 1])) : 0.f;
+          pp[j >> 1] = pack_bf16x2(p0, p1);
+          pd[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[j]) - dl[j]),
+                                   p1 * (__uint_as_float(dv[j + 1]) - dl[j + 1]));
+        }
+      }
+      tmem_st8(tmem + lane_base + kTmP + half * 64 + sc * 8, pp);
+      tmem_st8(tmem + lane_base + kTmDST + half * 64 + sc * 8, pd);
+      // dS (B operand of dQ^T, MN-major): tile row = key r, cols = q-rows
+      const uint32_t rowb = sbase + kSmDS + half * 16384 + r * 128;
+      const uint32_t c0 = uint32_t((2 * sc) ^ (r & 7)) * 16;
+      const uint32_t c1 = uint32_t((2 * sc + 1) ^ (r & 7)) * 16;
+      st_shared_v4(rowb + c0, pd[0], pd[1], pd[2], pd[3]);
+      st_shared_v4(rowb + c1, pd[4], pd[5], pd[6], pd[7]);
+    };
+    // Column scalars of task it+1 are loaded during task it (half 0 fills).
+    int4 rec1 = task_rec(tasks, 1, my_n, chunk);
+    float nl2 = 0.f, ndl = 0.f;
+    int njl = -1;
+    auto load_column = [&](const int4& rec, int64_t i) {
+      if (i >= my_n) return;
+      const TaskView tv = decode_task(rec);
+      const int qi = r >> 4, hh = r & 15;
+      const bool valid = qi < tv.nq;
+      const int32_t tok = task_token(p.col, tv, qi);
+      const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
+      int jl = tok - tv.key_start;
+      if (jl > tv.key_len - 1) jl = tv.key_len - 1;
+      njl = valid ? jl : -1;
+      nl2 = prm.lse[grow] * kLog2e;
+      ndl = prm.delta[grow];
+    };
+    if (half == 0) load_column(task_rec(tasks, 0, my_n, chunk), 0);
+    for (int64_t it = 0; it < my_n; ++it) {
+      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      named_bar_sync(1, 256);  // previous task's columns fully consumed
+      if (half == 0) {
+        s_lse2[r] = nl2;
+        s_delta[r] = ndl;
+        s_jlim[r] = int8_t(njl);
+        const bool wf = __all_sync(0xffffffffu, njl == kBlock - 1);
+        if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
+      }
+      named_bar_sync(1, 256);
+      if (half == 0) load_column(rec1, it + 1);  // in flight during this task
       if (!mbar_wait_warp(smem_u32(&bars.sdp_full), uint32_t(it & 1), abort_flag)) break;
       tc_fence_after();
+      const bool full = s_wfull[0] & s_wfull[1] & s_wfull[2] & s_wfull[3];
+      const uint32_t cS = tmem + lane_base + kTmS + half * 64;
+      const uint32_t cD = tmem + lane_base + kTmDP + half * 64;
+      uint32_t sA[16], dA[16], sB[16], dB[16];
+      tmem_ld16(cS, sA);
+      tmem_ld16(cD, dA);
+      tmem_ld_wait();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_base + kTmS + c * 32, sv);
-        tmem_ld32(tmem + lane_base + kTmDP + c * 32, dv);
+      for (int sp = 0; sp < 2; ++sp) {
+        const int sc0 = 2 * sp, sc1 = 2 * sp + 1;
+        tmem_ld16(cS + sc1 * 16, sB);
+        tmem_ld16(cD + sc1 * 16, dB);
+        sub_chunk(sc0, sA, dA, full);
         tmem_ld_wait();
-        uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int col = c * 32 + j;
-          const float p0 = (r <= s_jlim[col])
-                               ? fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -s_lse2[col]))
-                               : 0.f;
-          const float p1 =
-              (r <= s_jlim[col + 1])
-                  ? fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -s_lse2[col + 1]))
-                  : 0.f;
-          const float d0 = p0 * (__uint_as_float(dv[j]) - s_delta[col]);
-          const float d1 = p1 * (__uint_as_float(dv[j + 1]) - s_delta[col + 1]);
-          pp[j >> 1] = pack_bf16x2(p0, p1);
-          pd[j >> 1] = pack_bf16x2(d0, d1);
+        if (sp < 1) {
+          tmem_ld16(cS + (sc1 + 1) * 16, sA);
+          tmem_ld16(cD + (sc1 + 1) * 16, dA);
         }
-        // P^T over S^T cols [16c, 16c+16), dS^T over dP^T cols [128+16c, ...):
-        // both only cover columns this thread has already read.
-        tmem_st16(tmem + lane_base + kTmP + c * 16, pp);
-        tmem_st16(tmem + lane_base + kTmDST + c * 16, pd);
-        // dS (B operand of dQ^T, MN-major): tile row = key r, cols = q-rows
-        const uint32_t rowb = sbase + kSmDS + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t ch = (((c & 1) * 4 + u) ^ (r & 7)) * 16;
-          st_shared_v4(rowb + ch, pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
-        }
+        sub_chunk(sc1, sB, dB, full);
+        tmem_ld_wait();
       }
       tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.pds_full));
+      rec1 = rec2;
     }
   } else {
     // ---------------- reduce: dQ^T -> pool (thread = head dim), dV / dK flush
     const int quad = warp & 3;
     const int d = quad * 32 + lane;  // head dim = TMEM lane (dQ^T); key for dV / dK
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    const bool odd = lane & 1;
+    const bool issuer = (warp == 10 && lane == 0);
+    int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
     for (int64_t it = 0; it < my_n; ++it) {
-      const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
+      const TaskView tv = decode_task(rec);
+      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
       int32_t tok[kTaskQueries];
 #pragma unroll
-      for (int qi = 0; qi < kTaskQueries; ++qi)
-        tok[qi] = p.col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
+      for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = task_token(p.col, tv, qi);
       if (!mbar_wait_warp(smem_u32(&bars.dq_full), uint32_t(it & 1), abort_flag)) break;
       tc_fence_after();
-      uint32_t v[128];
+      const int64_t gb = int64_t(tv.g) * kHeadsPerGroup;
+      const int st = int(it & 1);
+      // dq_full(it) means every MMA of the task is complete, so the task's
+      // Q tile is free: stage the 16-bit dQ tile row-major in it, then one
+      // thread adds it to the pool with one bulk tensor reduction per query
+      // (16 heads x 128 dims = 4 KB) and hands the Q/dO stage back to the
+      // producer.  Even lanes write (row j, dims d, d+1), odd lanes (row j+1,
+      // dims d-1, d).
+      const uint32_t stage_base = sbase + kSmQ + st * kTileBytes;
+      const uint32_t stage = stage_base + uint32_t(odd ? 256 + 2 * (d - 1) : 2 * d);
+      auto consume = [&](const uint32_t (&v)[64], int j0) {
+        if (ACC == MSA_DQ_ACCUM_F32) {
+          float* pool = static_cast<float*>(prm.dq_pool) + d;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int jj = j0 + j;
+            if ((jj >> 4) < tv.nq)
+              red_add_f32(pool + ((int64_t(tok[jj >> 4]) * kQHeads + gb + (jj & 15)) * kHeadDim),
+                          __uint_as_float(v[j]) * prm.scale);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float a = __uint_as_float(v[j]) * prm.scale;
+            const float b = __uint_as_float(v[j + 1]) * prm.scale;
+            const float x = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const float lo = odd ? x : a, hi = odd ? b : x;
+            const uint32_t w2 =
+                ACC == MSA_DQ_ACCUM_F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+            const int jj = j0 + j;
+            st_shared_b32(stage + (jj >> 4) * 4096 + (jj & 15) * 256, w2);
+          }
+        }
+      };
+      uint32_t v[64];
       tmem_ld32(tmem + lane_base + kTmDQ + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(tmem + lane_base + kTmDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld32(tmem + lane_base + kTmDQ + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
-      tmem_ld32(tmem + lane_base + kTmDQ + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+      tmem_ld_wait();
+      consume(v, 0);
+      tmem_ld32(tmem + lane_base + kTmDQ + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem + lane_base + kTmDQ + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.dq_free));
-      const int64_t gbase = int64_t(tv.g) * kHeadsPerGroup;
-      if (prm.dq_accum == MSA_DQ_ACCUM_F32) {
-        float* pool = static_cast<float*>(prm.dq_pool);
-#pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const int qi = j >> 4;
-          if (qi < tv.nq) {
-            const int64_t row = int64_t(tok[qi]) * kQHeads + gbase + (j & 15);
-            red_add_f32(pool + row * kHeadDim + d, __uint_as_float(v[j]) * prm.scale);
-          }
+      consume(v, 64);
+      if (ACC != MSA_DQ_ACCUM_F32) {
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (issuer) {
+          for (int qi = 0; qi < tv.nq; ++qi)
+            tma_reduce_add_2d(&mapDQ, stage_base + qi * 4096, 0,
+                              tok[qi] * kQHeads + tv.g * kHeadsPerGroup);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(smem_u32(&bars.qdo_empty[st]));
         }
-      } else {
-        // even lanes reduce (row j, dims d, d+1), odd lanes (row j+1, dims d-1, d)
-        const bool odd = lane & 1;
-        uint16_t* pool = static_cast<uint16_t*>(prm.dq_pool);
-        const bool f16 = prm.dq_accum == MSA_DQ_ACCUM_F16;
-#pragma unroll
-        for (int j = 0; j < 128; j += 2) {
-          const float a = __uint_as_float(v[j]) * prm.scale;
-          const float b = __uint_as_float(v[j + 1]) * prm.scale;
-          const float x = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-          const int jr = odd ? j + 1 : j;
-          const int qi = jr >> 4;
-          if (qi < tv.nq) {
-            const int64_t row = int64_t(tok[qi]) * kQHeads + gbase + (jr & 15);
-            uint16_t* dst = pool + row * kHeadDim + (odd ? d - 1 : d);
-            const float lo = odd ? x : a, hi = odd ? b : x;
-            if (f16)
-              red_add_f16x2(dst, pack_f16x2(lo, hi));
-            else
-              red_add_bf16x2(dst, pack_bf16x2(lo, hi));
-          }
-        }
+      } else if (issuer) {
+        mbar_arrive(smem_u32(&bars.qdo_empty[st]));
       }
-      const bool seg_end =
-          (it + 1 == my_n) || decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub != tv.sub;
+      const bool seg_end = (it + 1 == my_n) || rec1.w != tv.sub;
       if (seg_end) {
-        // dq_full(it) follows dvdk_done(it): dV / dK of the run are final.
+        // dq_full(it) follows dv_done / dk_done(it): dV / dK of the run are final.
         const int key = d;
         const bool key_valid = key < tv.key_len;
         const int64_t krow = (int64_t(tv.key_start) + key) * kKVHeads + tv.g;
@@ -463,7 +572,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dkv_free));
       }
+      rec = rec1;
+      rec1 = rec2;
     }
+    if (issuer) bulk_wait0();  // bulk reductions complete before the CTA exits
   }
 
   if (threadIdx.x == 0 && abort_sh) raise_status(p.header, MSA_ERR_TIMEOUT);
@@ -524,6 +636,7 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
 
 CUresult make_map_rows(CUtensorMap* m, const void* base, int64_t rows);
 CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T);
+CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows, bool bf16);
 int device_sm_count();
 
 size_t backward_workspace_bytes(const msa_plan& p) { return bwd_layout(p).total; }
@@ -538,10 +651,15 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   float* dk_pool = reinterpret_cast<float*>(w + L.off_dk);
   float* dv_pool = reinterpret_cast<float*>(w + L.off_dv);
 
-  CUtensorMap mQ, mDO, mK, mV;
+  CUtensorMap mQ, mDO, mK, mV, mDQ;
+  memset(&mDQ, 0, sizeof mDQ);
   if (make_map_rows(&mQ, q, p.T * kQHeads) != CUDA_SUCCESS ||
       make_map_rows(&mDO, dout, p.T * kQHeads) != CUDA_SUCCESS ||
       make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (p.dq_accum != MSA_DQ_ACCUM_F32 &&
+      make_map_pool16(&mDQ, dq_pool, p.T * kQHeads, p.dq_accum == MSA_DQ_ACCUM_BF16) !=
+          CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   const int64_t rows = p.T * kQHeads;
@@ -557,15 +675,23 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
 
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {k_bwd_main<MSA_DQ_ACCUM_F16>, k_bwd_main<MSA_DQ_ACCUM_BF16>,
+                    k_bwd_main<MSA_DQ_ACCUM_F32>}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 16,
                 p.dq_accum};
   launch_begin("bwd_main", s);
-  k_bwd_main<<<unsigned(device_sm_count()), kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
+  const unsigned grid = unsigned(device_sm_count());
+  if (p.dq_accum == MSA_DQ_ACCUM_F32)
+    k_bwd_main<MSA_DQ_ACCUM_F32><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
+  else if (p.dq_accum == MSA_DQ_ACCUM_BF16)
+    k_bwd_main<MSA_DQ_ACCUM_BF16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
+  else
+    k_bwd_main<MSA_DQ_ACCUM_F16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
   launch_end("bwd_main", s);
   launch_begin("bwd_finalize", s);
   k_bwd_finalize<<<unsigned(device_sm_count() * 8), 256, 0, s>>>(

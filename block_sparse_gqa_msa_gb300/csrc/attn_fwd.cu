@@ -8,12 +8,14 @@
 // bucket and each tile is a dense 128x128x128 tensor-core contraction.
 //
 // The up-to-16 partial results of a row (one per selected block) are merged
-// without a second pass over the scores: every task exponentiates against
-// the same per-row shift M[t,h] = scale * |q_th| * max_{selected v} max_{j in v}
-// |k_jg| (log2 units), which bounds every score of the row (Cauchy-Schwarz),
-// and adds its unnormalised P.V and row sum into fp32 pools with L2
-// reductions.  The finalize divides.  Rows whose sum underflows (the bound far
-// above the true maximum) are recomputed exactly by a fallback kernel.
+// without a second pass over the scores.  Each task exponentiates against its
+// own tile row maximum m (P = exp(s - m) in (0, 1], fp16 for the P.V product)
+// and rescales its partial P.V and row sum by exp(m - M) onto a per-row shift
+// M[t,h] = scale * |q_th| * max_{selected v} max_{j in v} |k_jg| shared by all
+// tasks of the row; M bounds every score of the row (Cauchy-Schwarz), so the
+// rescaled partials add up in fp32 pools with L2 bulk reductions.  The
+// finalize divides.  Rows whose sum underflows (the bound far above the true
+// maximum) are recomputed exactly by a fallback kernel.
 //
 // Kernels, in launch order:
 //   fwd_kmax      per (index head, key block): max key norm
@@ -34,7 +36,7 @@ constexpr float kUnderflowSum = 8.673617379884035e-19f;
 
 // ------------------------------------------------------------ workspace
 struct FwdLayout {
-  size_t off_m, off_l, off_l2, off_pool, off_kmax, off_vmax, off_list, total;
+  size_t off_m, off_l, off_pool, off_kmax, off_vmax, off_list, total;
 };
 FwdLayout fwd_layout(const msa_plan& p) {
   FwdLayout L{};
@@ -42,7 +44,6 @@ FwdLayout fwd_layout(const msa_plan& p) {
   size_t o = 0;
   L.off_m = o;    o = align_up(o + sizeof(float) * rows, 256);
   L.off_l = o;    o = align_up(o + sizeof(float) * rows, 256);
-  L.off_l2 = o;   o = align_up(o + sizeof(float) * rows, 256);
   L.off_pool = o; o = align_up(o + sizeof(float) * rows * kHeadDim, 256);
   L.off_kmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
   L.off_vmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat1
 // heads (-inf when the row sees no key), and zero the row's pool and sum.
 __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat16* Q,
                                                   const float* kmax, float c2, float* M2,
-                                                  float* lsum, float* lsum2, float* pool) {
+                                                  float* lsum, float* pool) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
@@ -184,7 +185,6 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
       const int64_t row = t * kQHeads + g * kHeadsPerGroup + hh;
       M2[row] = km < 0.f ? -INFINITY : c2 * sqrtf(s) * km;
       lsum[row] = 0.f;
-      lsum2[row] = 0.f;
     }
   }
   float4* z = reinterpret_cast<float4*>(prow);
@@ -194,24 +194,27 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
 }
 
 // ------------------------------------------------------------ fwd_main
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-5 softmax +
-// epilogue (thread = tile row = TMEM lane), 6 converts each V tile to fp16.
-// TMEM: S in columns [0,128) / [128,256) (two stages), O_part in
-// [256,384) / [384,512).
-//
-// Per task the softmax works relative to the tile's own row maximum m
-// (P = exp(s - m) in (0, 1], fp16), and the epilogue rescales the partial
-// P.V and row sums by exp(m - M) before adding them to the pools, so every
-// task of a row lands on the same shift M.
-constexpr int kFwdThreads = 224;
+// Warp roles (352 threads):
+//   0     TMA producer: K/V per block run, Q per task (two stages)
+//   1     MMA issuer (TMEM owner): S = Q K^T, O_part = P V with P read from TMEM
+//   2-5   softmax (thread = tile row = TMEM lane): row max, P = exp(s - m) as
+//         fp16 written over the row's S columns, row sum
+//   6-9   epilogue (thread = tile row): O_part * exp(m - M) staged in shared
+//         memory and added to the fp32 pool by one 512 B bulk reduction per
+//         row; row sums by atomics
+//   10    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
+// TMEM: S (and P over its first 64 columns) in [0,128) / [128,256), O_part in
+// [256,384) / [384,512), two stages each.
+constexpr int kFwdThreads = 352;
 constexpr uint32_t kTileBytes = 32768;
-constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmP = 131072, kSmStage = 163840;
-constexpr uint32_t kStageFloats = 32 * 33;
-constexpr uint32_t kFwdSmem = kSmStage + 4 * kStageFloats * 4 + 1024;
+constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
+constexpr uint32_t kStageRowBytes = 528;  // 512 B of data + 16 B pad
+constexpr uint32_t kStageBytes = 128 * kStageRowBytes;
+constexpr uint32_t kFwdSmem = kSmStage + kStageBytes + 1024;
 
 struct FwdBars {
-  uint64_t kv_full, kv_empty, v_ready, q_full[2], q_empty[2], s_full[2], s_free[2], p_full,
-      p_free, o_full[2], o_free[2], fin;
+  uint64_t kv_full, kv_empty, v_ready, q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2],
+      o_free[2], fin;
 };
 
 struct FwdParams {
@@ -219,8 +222,7 @@ struct FwdParams {
   const float* M2;
   const float* vmax;
   float* pool;
-  float* lsum;   // sum of the fp32 weights (gives LSE)
-  float* lsum2;  // sum of the fp16-rounded weights (normalises O)
+  float* lsum;
   float c2;
   int chunk;
 };
@@ -238,29 +240,11 @@ __device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
   return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
                                                                     : chunk);
 }
-
-// Reduce 32 rows x 32 fp32 columns held one row per lane into global rows
-// (one destination pointer per lane, already offset to the column chunk)
-// with coalesced 16-byte L2 reductions; the warp transposes through `stage`.
-__device__ __forceinline__ void warp_reduce_rows(float* stage, const uint32_t (&r)[32], float mul,
-                                                 float* dst, bool valid) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]) * mul;
-  __syncwarp();
-#pragma unroll
-  for (int rr = 0; rr < 32; rr += 4) {
-    const int src = rr + (lane >> 3);
-    const int c4 = (lane & 7) * 4;
-    float* d = reinterpret_cast<float*>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), src));
-    const bool v = __shfl_sync(0xffffffffu, valid ? 1 : 0, src) != 0;
-    if (v) {
-      const float* sp = stage + src * 33 + c4;
-      red_add_v4_f32(d + c4, sp[0], sp[1], sp[2], sp[3]);
-    }
-  }
-  __syncwarp();
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n, int chunk) {
+  return i < n ? tasks[cta_task(i, chunk)] : make_int4(0, 0, 1 << 8, -1);
+}
+__device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
+  return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
 }
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -270,6 +254,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __shared__ FwdBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
+  __shared__ float s_alpha[2][128], s_lrow[2][128];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -287,12 +272,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&bars.q_full[i]), 1);
       mbar_init(smem_u32(&bars.q_empty[i]), 1);
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.s_free[i]), 128);
+      mbar_init(smem_u32(&bars.p_full[i]), 128);
       mbar_init(smem_u32(&bars.o_full[i]), 1);
       mbar_init(smem_u32(&bars.o_free[i]), 128);
     }
-    mbar_init(smem_u32(&bars.p_full), 128);
-    mbar_init(smem_u32(&bars.p_free), 1);
     mbar_init(smem_u32(&bars.fin), 1);
     fence_mbar_init();
   }
@@ -307,17 +290,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
   const int64_t my_n = cta_task_count(ntasks, prm.chunk);
   const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
+  const int chunk = prm.chunk;
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (records and tokens prefetched one task ahead)
     if (lane == 0 && my_n > 0) {
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
+      int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+      int32_t tok[kTaskQueries];
+      {
+        const TaskView tv = decode_task(rec);
+#pragma unroll
+        for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = task_token(p.col, tv, qi);
+      }
       for (; it < my_n; ++it) {
-        const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
+        const TaskView tv = decode_task(rec);
+        const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+        int32_t tok1[kTaskQueries];
+        {
+          const TaskView tv1 = decode_task(rec1);
+#pragma unroll
+          for (int qi = 0; qi < kTaskQueries; ++qi)
+            tok1[qi] = it + 1 < my_n ? task_token(p.col, tv1, qi) : 0;
+        }
         if (tv.sub != prev_kv) {
           if (kv_loads > 0 &&
               !mbar_wait(smem_u32(&bars.kv_empty), uint32_t((kv_loads - 1) & 1), abort_flag))
@@ -338,12 +337,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t b = smem_u32(&bars.q_full[st]);
         mbar_arrive_expect_tx(b, kTileBytes);
         const uint32_t dst = sbase + kSmQ + st * kTileBytes;
+#pragma unroll
         for (int qi = 0; qi < kTaskQueries; ++qi) {
-          const int32_t tok = p.col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
-          const int y = tok * kQHeads + tv.g * kHeadsPerGroup;
+          const int y = tok[qi] * kQHeads + tv.g * kHeadsPerGroup;
           tma_load_2d(dst + qi * 2048, &mapQ, b, 0, y);
           tma_load_2d(dst + 16384 + qi * 2048, &mapQ, b, 64, y);
         }
+        rec = rec1;
+        rec1 = rec2;
+#pragma unroll
+        for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = tok1[qi];
       }
       if (*abort_flag) {  // let armed copies land before the CTA exits
         if (kv_loads > 0) mbar_wait_drain(smem_u32(&bars.kv_full), uint32_t((kv_loads - 1) & 1));
@@ -355,15 +358,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ---------------- MMA issuer
     if (lane == 0 && my_n > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T   (bf16)
-      constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, V MN-major)
+      constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, P in TMEM)
       int64_t kv_loads = 0;
       bool ok = true, need_v = false;
+      // S(it) goes to stage it&1, whose P(it-2) must have been read by PV(it-2).
       auto issue_S = [&](int64_t it) -> bool {
         const int st = int(it & 1);
         if (!mbar_wait(smem_u32(&bars.q_full[st]), uint32_t((it >> 1) & 1), abort_flag))
           return false;
         if (it >= 2 &&
-            !mbar_wait(smem_u32(&bars.s_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
+            !mbar_wait(smem_u32(&bars.o_full[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
           return false;
         tc_fence_after();
         const uint32_t sq = sbase + kSmQ + st * kTileBytes;
@@ -381,15 +385,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         need_v = true;
         return true;
       };
-      int cur_kv = decode_task(tasks[cta_task(0, prm.chunk)]).sub;
+      int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
+      int next_kv = task_rec(tasks, 1, my_n, chunk).w;
       ok = wait_kv() && issue_S(0);
       for (int64_t it = 0; ok && it < my_n; ++it) {
         const int st = int(it & 1);
-        int next_kv = -1;
-        if (it + 1 < my_n) next_kv = decode_task(tasks[cta_task(it + 1, prm.chunk)]).sub;
+        const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;
         const bool same = (it + 1 < my_n) && next_kv == cur_kv;
         if (same && !issue_S(it + 1)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars.p_full), uint32_t(it & 1), abort_flag)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars.p_full[st]), uint32_t((it >> 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
         if (it >= 2 &&
             !mbar_wait(smem_u32(&bars.o_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag)) {
           ok = false;
@@ -405,32 +412,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + 256 + st * 128, desc_kmajor(sbase + kSmP, kk),
-                  desc_mnmajor(sbase + kSmV, kk), idPV, kk > 0);
+          umma_ts(tmem + 256 + st * 128, tmem + st * 128 + kk * 8, desc_mnmajor(sbase + kSmV, kk),
+                  idPV, kk > 0);
         umma_commit(smem_u32(&bars.o_full[st]));
-        umma_commit(smem_u32(&bars.p_free));
         if (it + 1 < my_n && !same) {
           umma_commit(smem_u32(&bars.kv_empty));
           cur_kv = next_kv;
           if (!wait_kv() || !issue_S(it + 1)) { ok = false; break; }
         }
+        next_kv = next2_kv;
       }
       // Make sure no MMA is still running before TMEM is released.
       umma_commit(smem_u32(&bars.fin));
       mbar_wait_drain(smem_u32(&bars.fin), 0);
     }
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // ---------------- V tile bf16 -> fp16 (scaled by an exact power of two)
     if (my_n > 0) {
       int prev_kv = -1;
       int64_t kv_loads = 0;
       for (int64_t it = 0; it < my_n; ++it) {
-        const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-        if (tv.sub == prev_kv) continue;
-        prev_kv = tv.sub;
+        const int kv = task_rec(tasks, it, my_n, chunk).w;
+        if (kv == prev_kv) continue;
+        prev_kv = kv;
+        const float sc = v_scale_in(prm.vmax[kv]);
         if (!mbar_wait_warp(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) break;
         ++kv_loads;
-        const float sc = v_scale_in(prm.vmax[tv.sub]);
         for (int i = lane; i < 2048; i += 32) {
           const uint32_t a = sbase + kSmV + i * 16;
           const uint4 x = ld_shared_v4(a);
@@ -444,46 +451,71 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bars.v_ready));
       }
     }
-  } else {
-    // ---------------- softmax + epilogue (warps 2-5)
-    const int quad = warp & 3;            // TMEM lane quadrant of this warp
-    const int row = quad * 32 + lane;     // tile row = TMEM lane
+  } else if (warp < 6) {
+    // ---------------- softmax (warps 2-5)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    float* stage = reinterpret_cast<float*>(smem + kSmStage) + (warp - 2) * kStageFloats;
+    const int qi = row >> 4, hh = row & 15;
+    // row data of task it+1 is loaded during task it
+    int njmax = -1;
+    float nm2 = 0.f;
+    auto load_row = [&](const int4& rec, int64_t i) {
+      if (i >= my_n) return;
+      const TaskView tv = decode_task(rec);
+      const int32_t tok = task_token(p.col, tv, qi);
+      int jm = tok - tv.key_start;
+      if (jm > tv.key_len - 1) jm = tv.key_len - 1;
+      njmax = qi < tv.nq ? jm : -1;
+      nm2 = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
+    };
+    int4 rec1 = task_rec(tasks, 1, my_n, chunk);
+    load_row(task_rec(tasks, 0, my_n, chunk), 0);
     for (int64_t it = 0; it < my_n; ++it) {
       const int st = int(it & 1);
-      const TaskView tv = decode_task(tasks[cta_task(it, prm.chunk)]);
-      const int qi = row >> 4, hh = row & 15;
-      const bool row_valid = qi < tv.nq;
-      const int32_t tok = p.col[tv.col_begin + (row_valid ? qi : tv.nq - 1)];
-      const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      int jmax = tok - tv.key_start;
-      if (jmax > tv.key_len - 1) jmax = tv.key_len - 1;
-      if (!row_valid) jmax = -1;
-      const float m2 = prm.M2[grow];
-      const float vs = v_scale_in(prm.vmax[tv.sub]);
+      const int jmax = njmax;
+      const float m2 = nm2;
+      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      load_row(rec1, it + 1);
       if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       tc_fence_after();
+      const uint32_t cs = tmem + lane_base + st * 128;
       // pass 1: the tile row's maximum over visible keys (raw scores)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + st * 128 + c * 32, r);
+      // (eight independent running maxima keep the dependency chains short)
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+      {
+        uint32_t a[32], b[32];
+        tmem_ld32(cs, a);
+        tmem_ld32(cs + 32, b);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c * 32 + j <= jmax) mx = fmaxf(mx, __uint_as_float(r[j]));
+        for (int j = 0; j < 32; ++j) {
+          if (j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(a[j]));
+          if (32 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(b[j]));
+        }
+        tmem_ld32(cs + 64, a);
+        tmem_ld32(cs + 96, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (64 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(a[j]));
+          if (96 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(b[j]));
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mxc = (jmax >= 0) ? mx * prm.c2 : 0.f;
-      if (it >= 1 && !mbar_wait_warp(smem_u32(&bars.p_free), uint32_t((it - 1) & 1), abort_flag))
-        break;
-      // pass 2: P = exp(s - m) as fp16 into the P tile; exact and rounded sums
-      float l_exact = 0.f, l_round = 0.f;
+      // pass 2: P = exp(s - m) as fp16 pairs over S columns [16c, 16c+16)
+      // (columns already read); row sum of the fp32 values
+      float ls8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_base + st * 128 + c * 32, r);
+        tmem_ld32(cs + c * 32, r);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -492,42 +524,84 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float x0 = (k0 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j]), prm.c2, -mxc)) : 0.f;
           const float x1 =
               (k0 + 1 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j + 1]), prm.c2, -mxc)) : 0.f;
-          const uint32_t w2 = pack_f16x2(x0, x1);
-          l_exact += x0 + x1;
-          l_round += f16_lo(w2) + f16_hi(w2);
-          pk[j >> 1] = w2;
+          ls8[(j >> 1) & 7] += x0 + x1;
+          pk[j >> 1] = pack_f16x2(x0, x1);
         }
-        const uint32_t prow = sbase + kSmP + (c >> 1) * 16384 + row * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t chunk = ((c & 1) * 4 + u) ^ (row & 7);
-          st_shared_v4(prow + chunk * 16, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        tmem_st16(cs + c * 16, pk);
       }
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      // the epilogue of task it-2 has read this stage's row scalars once it
+      // released O_part (o_free)
+      if (it >= 2 &&
+          !mbar_wait_warp(smem_u32(&bars.o_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
+        break;
+      s_alpha[st][row] = jmax >= 0 ? fast_exp2(mxc - m2) : 0.f;
+      s_lrow[st][row] = lsum;
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.s_free[st]));
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bars.p_full));
-
-      // epilogue: pool[row] += exp(m - M) * O_partial / vscale
-      const float alpha = row_valid ? fast_exp2(mxc - m2) : 0.f;
-      if (!mbar_wait_warp(smem_u32(&bars.o_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
-      tc_fence_after();
-      float* dst_row = prm.pool + grow * kHeadDim;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + 256 + st * 128 + c * 32, r);
-        tmem_ld_wait();
-        warp_reduce_rows(stage, r, alpha / vs, dst_row + c * 32, row_valid);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.o_free[st]));
-      if (row_valid) {
-        atomicAdd(prm.lsum + grow, alpha * l_exact);
-        atomicAdd(prm.lsum2 + grow, alpha * l_round);
-      }
+      mbar_arrive(smem_u32(&bars.p_full[st]));
+      rec1 = rec2;
     }
+  } else {
+    // ---------------- epilogue (warps 6-9)
+    // Each thread owns one tile row: it stages its scaled 128-float row in
+    // shared memory (rows padded to 528 B so the lanes of a wavefront hit
+    // different banks) and adds it to the pool with one 512 B bulk reduction.
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    const int qi = row >> 4, hh = row & 15;
+    const uint32_t stage_row = sbase + kSmStage + uint32_t(row) * kStageRowBytes;
+    int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    bool pending = false;
+    for (int64_t it = 0; it < my_n; ++it) {
+      const int st = int(it & 1);
+      const TaskView tv = decode_task(rec);
+      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      const int32_t tok = task_token(p.col, tv, qi);
+      const bool valid = qi < tv.nq;
+      const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
+      const float vs_inv = 1.f / v_scale_in(prm.vmax[tv.sub]);
+      if (!mbar_wait_warp(smem_u32(&bars.o_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
+      // p_full(it) completed before o_full(it); waiting on it makes the
+      // softmax's row scalars visible here.
+      if (!mbar_wait_warp(smem_u32(&bars.p_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
+      tc_fence_after();
+      const float alpha = s_alpha[st][row];
+      const float lrow = s_lrow[st][row];
+      const float mul = alpha * vs_inv;
+      if (pending) bulk_wait_read0();  // this row's previous bulk reduction read the stage
+      uint32_t v[64];
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld32(tmem + lane_base + 256 + st * 128 + h * 64,
+                  *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tmem + lane_base + 256 + st * 128 + h * 64 + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        if (h == 1) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.o_free[st]));
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          st_shared_v4(stage_row + h * 256 + u * 16,
+                       __float_as_uint(__uint_as_float(v[4 * u + 0]) * mul),
+                       __float_as_uint(__uint_as_float(v[4 * u + 1]) * mul),
+                       __float_as_uint(__uint_as_float(v[4 * u + 2]) * mul),
+                       __float_as_uint(__uint_as_float(v[4 * u + 3]) * mul));
+      }
+      if (valid) {
+        fence_proxy_async_smem();
+        bulk_reduce_add_f32(prm.pool + grow * kHeadDim, stage_row, kHeadDim * 4);
+        bulk_commit();
+        pending = true;
+        atomicAdd(prm.lsum + grow, alpha * lrow);
+      }
+      rec = rec1;
+      rec1 = rec2;
+    }
+    if (pending) bulk_wait0();  // bulk reductions complete before the CTA exits
   }
 
   // ---------------- teardown
@@ -540,9 +614,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ------------------------------------------------------------ fwd_finalize
 // One warp per row (t, h).
 __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M2,
-                                                      const float* lsum, const float* lsum2,
-                                                      const float* pool, __nv_bfloat16* O,
-                                                      float* lse, int32_t* list) {
+                                                      const float* lsum, const float* pool,
+                                                      __nv_bfloat16* O, float* lse,
+                                                      int32_t* list) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (row >= p.T * kQHeads) return;
@@ -561,7 +635,7 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
       }
     } else {
       const float4 x = reinterpret_cast<const float4*>(pool + row * kHeadDim)[lane];
-      const float inv = 1.f / lsum2[row];
+      const float inv = 1.f / l;
       out.x = pack_bf16x2(x.x * inv, x.y * inv);
       out.y = pack_bf16x2(x.z * inv, x.w * inv);
       L = (m2 + __log2f(l)) * kLn2;
@@ -648,7 +722,6 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* M2 = reinterpret_cast<float*>(w + L.off_m);
   float* lsum = reinterpret_cast<float*>(w + L.off_l);
-  float* lsum2 = reinterpret_cast<float*>(w + L.off_l2);
   float* vmax = reinterpret_cast<float*>(w + L.off_vmax);
   float* pool = reinterpret_cast<float*>(w + L.off_pool);
   float* kmax = reinterpret_cast<float*>(w + L.off_kmax);
@@ -669,7 +742,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
   k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, c2, M2, lsum, lsum2, pool);
+      p, static_cast<const __nv_bfloat16*>(q), kmax, c2, M2, lsum, pool);
   launch_end("fwd_rows", s);
 
   static bool attr_set = false;
@@ -678,14 +751,14 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  FwdParams prm{p, M2, vmax, pool, lsum, lsum2, c2, 8};
+  FwdParams prm{p, M2, vmax, pool, lsum, c2, 8};
   launch_begin("fwd_main", s);
   k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV);
   launch_end("fwd_main", s);
   const int64_t rows = p.T * kQHeads;
   launch_begin("fwd_finalize", s);
   k_fwd_finalize<<<unsigned((rows + 7) / 8), 256, 0, s>>>(
-      p, M2, lsum, lsum2, pool, static_cast<__nv_bfloat16*>(o), lse, list);
+      p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o), lse, list);
   launch_end("fwd_finalize", s);
   launch_begin("fwd_fallback", s);
   k_fwd_fallback<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(
