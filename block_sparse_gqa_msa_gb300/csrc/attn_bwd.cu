@@ -409,36 +409,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       st_shared_v4(rowb + c0, pd[0], pd[1], pd[2], pd[3]);
       st_shared_v4(rowb + c1, pd[4], pd[5], pd[6], pd[7]);
     };
-    // Column scalars of task it+1 are loaded during task it (half 0 fills).
+    // Column scalars of task it+1 are loaded while task it is computed, in
+    // two steps so no load result is consumed right after it is issued: the
+    // column's token at the top of task it, its LSE / delta mid-way.
+    const int qi = r >> 4, hh = r & 15;
     int4 rec1 = task_rec(tasks, 1, my_n, chunk);
-    float nl2 = 0.f, ndl = 0.f;
-    int njl = -1;
-    auto load_column = [&](const int4& rec, int64_t i) {
-      if (i >= my_n) return;
-      const TaskView tv = decode_task(rec);
-      const int qi = r >> 4, hh = r & 15;
-      const bool valid = qi < tv.nq;
+    float cl2 = 0.f, cdl = 0.f;  // current task's column values
+    int cjl = -1;
+    if (half == 0 && my_n > 0) {
+      const TaskView tv = decode_task(task_rec(tasks, 0, my_n, chunk));
       const int32_t tok = task_token(p.col, tv, qi);
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      int jl = tok - tv.key_start;
-      if (jl > tv.key_len - 1) jl = tv.key_len - 1;
-      njl = valid ? jl : -1;
-      nl2 = prm.lse[grow] * kLog2e;
-      ndl = prm.delta[grow];
-    };
-    if (half == 0) load_column(task_rec(tasks, 0, my_n, chunk), 0);
+      cjl = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
+      cl2 = prm.lse[grow] * kLog2e;
+      cdl = prm.delta[grow];
+    }
     for (int64_t it = 0; it < my_n; ++it) {
       const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      int32_t ntok = 0;
+      if (half == 0 && it + 1 < my_n) ntok = task_token(p.col, decode_task(rec1), qi);
       named_bar_sync(1, 256);  // previous task's columns fully consumed
       if (half == 0) {
-        s_lse2[r] = nl2;
-        s_delta[r] = ndl;
-        s_jlim[r] = int8_t(njl);
-        const bool wf = __all_sync(0xffffffffu, njl == kBlock - 1);
+        s_lse2[r] = cl2;
+        s_delta[r] = cdl;
+        s_jlim[r] = int8_t(cjl);
+        const bool wf = __all_sync(0xffffffffu, cjl == kBlock - 1);
         if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
       }
       named_bar_sync(1, 256);
-      if (half == 0) load_column(rec1, it + 1);  // in flight during this task
       if (!mbar_wait_warp(smem_u32(&bars.sdp_full), uint32_t(it & 1), abort_flag)) break;
       tc_fence_after();
       const bool full = s_wfull[0] & s_wfull[1] & s_wfull[2] & s_wfull[3];
@@ -458,6 +456,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (sp < 1) {
           tmem_ld16(cS + (sc1 + 1) * 16, sA);
           tmem_ld16(cD + (sc1 + 1) * 16, dA);
+          if (half == 0 && it + 1 < my_n) {  // next task's column values
+            const TaskView tn = decode_task(rec1);
+            const int64_t grow = int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh;
+            cjl = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
+            cl2 = prm.lse[grow] * kLog2e;
+            cdl = prm.delta[grow];
+          }
         }
         sub_chunk(sc1, sB, dB, full);
         tmem_ld_wait();

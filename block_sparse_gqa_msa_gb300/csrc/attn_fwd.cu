@@ -194,18 +194,19 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
 }
 
 // ------------------------------------------------------------ fwd_main
-// Warp roles (352 threads):
+// Warp roles (480 threads):
 //   0     TMA producer: K/V per block run, Q per task (two stages)
 //   1     MMA issuer (TMEM owner): S = Q K^T, O_part = P V with P read from TMEM
-//   2-5   softmax (thread = tile row = TMEM lane): row max, P = exp(s - m) as
-//         fp16 written over the row's S columns, row sum
-//   6-9   epilogue (thread = tile row): O_part * exp(m - M) staged in shared
+//   2-9   softmax (thread = tile row = TMEM lane): row max, P = exp(s - m) as
+//         fp16 written over the row's S columns, row sum; warps 2-5 take the
+//         even tasks (TMEM stage 0), warps 6-9 the odd ones (stage 1)
+//   10-13 epilogue (thread = tile row): O_part * exp(m - M) staged in shared
 //         memory and added to the fp32 pool by one 512 B bulk reduction per
 //         row; row sums by atomics
-//   10    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
+//   14    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
 // TMEM: S (and P over its first 64 columns) in [0,128) / [128,256), O_part in
 // [256,384) / [384,512), two stages each.
-constexpr int kFwdThreads = 352;
+constexpr int kFwdThreads = 480;
 constexpr uint32_t kTileBytes = 32768;
 constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
 constexpr uint32_t kStageRowBytes = 528;  // 512 B of data + 16 B pad
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       umma_commit(smem_u32(&bars.fin));
       mbar_wait_drain(smem_u32(&bars.fin), 0);
     }
-  } else if (warp == 10) {
+  } else if (warp == 14) {
     // ---------------- V tile bf16 -> fp16 (scaled by an exact power of two)
     if (my_n > 0) {
       int prev_kv = -1;
@@ -451,32 +452,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bars.v_ready));
       }
     }
-  } else if (warp < 6) {
-    // ---------------- softmax (warps 2-5)
+  } else if (warp < 10) {
+    // ---------------- softmax (warps 2-5: even tasks, 6-9: odd tasks)
     const int quad = warp & 3;
+    const int par = (warp - 2) >> 2;
     const int row = quad * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
     const int qi = row >> 4, hh = row & 15;
-    // row data of task it+1 is loaded during task it
-    int njmax = -1;
-    float nm2 = 0.f;
-    auto load_row = [&](const int4& rec, int64_t i) {
-      if (i >= my_n) return;
-      const TaskView tv = decode_task(rec);
+    // Row data of this warpgroup's next task (it+2) is loaded while task it
+    // runs, in two steps so no load result is consumed right after it is
+    // issued: the row's token at the top of task it, its shift M after the
+    // exponentials.
+    int4 rec1 = task_rec(tasks, par + 2, my_n, chunk);
+    int jmax_c = -1;
+    float m2_c = 0.f;
+    if (par < my_n) {
+      const TaskView tv = decode_task(task_rec(tasks, par, my_n, chunk));
       const int32_t tok = task_token(p.col, tv, qi);
-      int jm = tok - tv.key_start;
-      if (jm > tv.key_len - 1) jm = tv.key_len - 1;
-      njmax = qi < tv.nq ? jm : -1;
-      nm2 = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
-    };
-    int4 rec1 = task_rec(tasks, 1, my_n, chunk);
-    load_row(task_rec(tasks, 0, my_n, chunk), 0);
-    for (int64_t it = 0; it < my_n; ++it) {
+      jmax_c = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
+      m2_c = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
+    }
+    for (int64_t it = par; it < my_n; it += 2) {
       const int st = int(it & 1);
-      const int jmax = njmax;
-      const float m2 = nm2;
-      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
-      load_row(rec1, it + 1);
+      const int jmax = jmax_c;
+      const float m2 = m2_c;
+      const int4 rec2 = task_rec(tasks, it + 4, my_n, chunk);
+      const int32_t ntok = it + 2 < my_n ? task_token(p.col, decode_task(rec1), qi) : 0;
       if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       tc_fence_after();
       const uint32_t cs = tmem + lane_base + st * 128;
@@ -530,6 +531,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st16(cs + c * 16, pk);
       }
       const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      if (it + 2 < my_n) {  // this warpgroup's next task
+        const TaskView tn = decode_task(rec1);
+        jmax_c = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
+        m2_c = prm.M2[int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh];
+      }
       // the epilogue of task it-2 has read this stage's row scalars once it
       // released O_part (o_free)
       if (it >= 2 &&
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       rec1 = rec2;
     }
   } else {
-    // ---------------- epilogue (warps 6-9)
+    // ---------------- epilogue (warps 10-13)
     // Each thread owns one tile row: it stages its scaled 128-float row in
     // shared memory (rows padded to 528 B so the lanes of a wavefront hit
     // different banks) and adds it to the pool with one 512 B bulk reduction.
@@ -554,14 +560,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t stage_row = sbase + kSmStage + uint32_t(row) * kStageRowBytes;
     int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
     bool pending = false;
+    // the row's token and the block's V scale are loaded one task ahead
+    int32_t tok_c = my_n > 0 ? task_token(p.col, decode_task(rec), qi) : 0;
+    float vmax_c = my_n > 0 ? prm.vmax[rec.w] : 0.f;
     for (int64_t it = 0; it < my_n; ++it) {
       const int st = int(it & 1);
       const TaskView tv = decode_task(rec);
       const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
-      const int32_t tok = task_token(p.col, tv, qi);
+      const int32_t tok = tok_c;
+      const float vmx = vmax_c;
+      if (it + 1 < my_n) {
+        tok_c = task_token(p.col, decode_task(rec1), qi);
+        vmax_c = prm.vmax[rec1.w];
+      }
       const bool valid = qi < tv.nq;
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      const float vs_inv = 1.f / v_scale_in(prm.vmax[tv.sub]);
       if (!mbar_wait_warp(smem_u32(&bars.o_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       // p_full(it) completed before o_full(it); waiting on it makes the
       // softmax's row scalars visible here.
@@ -569,7 +582,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const float alpha = s_alpha[st][row];
       const float lrow = s_lrow[st][row];
-      const float mul = alpha * vs_inv;
+      const float mul = alpha / v_scale_in(vmx);
       if (pending) bulk_wait_read0();  // this row's previous bulk reduction read the stage
       uint32_t v[64];
 #pragma unroll 1
@@ -612,38 +625,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 // ------------------------------------------------------------ fwd_finalize
-// One warp per row (t, h).
+// O = pool / sum -> bf16 and LSE = (M + log2 sum) ln 2.  Each warp finishes
+// eight rows per step (16 lanes x 8 elements per row), all loads issued
+// before any use.  Rows whose sum underflowed are listed for the fallback.
+constexpr int kFinRowsPerWarp = 8;
 __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M2,
                                                       const float* lsum, const float* pool,
                                                       __nv_bfloat16* O, float* lse,
                                                       int32_t* list) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (row >= p.T * kQHeads) return;
   if (plan_failed(p.header)) return;
-  const float m2 = M2[row];
-  const float l = lsum[row];
-  uint2 out = make_uint2(0u, 0u);
-  bool write = true;
-  float L = -INFINITY;
-  if (m2 != -INFINITY) {
-    if (!(l >= kUnderflowSum) || !isfinite(l)) {
-      write = false;  // the fallback kernel writes this row
-      if (lane == 0) {
-        const int32_t k = atomicAdd(list, 1);
-        list[1 + k] = int32_t(row);
+  const int lane = threadIdx.x & 31, sub = lane & 15;
+  const int64_t rows = p.T * kQHeads;
+  const int64_t nwarps = int64_t(gridDim.x) * blockDim.x / 32;
+  for (int64_t r0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32 * kFinRowsPerWarp;
+       r0 < rows; r0 += nwarps * kFinRowsPerWarp) {
+    float4 a[4], b[4];
+    float m2[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + 2 * i + (lane >> 4);
+      if (row < rows) {
+        const float4* src = reinterpret_cast<const float4*>(pool + row * kHeadDim) + 2 * sub;
+        a[i] = src[0];
+        b[i] = src[1];
+        m2[i] = M2[row];
+        l[i] = lsum[row];
+      } else {
+        m2[i] = -INFINITY;
+        l[i] = 0.f;
       }
-    } else {
-      const float4 x = reinterpret_cast<const float4*>(pool + row * kHeadDim)[lane];
-      const float inv = 1.f / l;
-      out.x = pack_bf16x2(x.x * inv, x.y * inv);
-      out.y = pack_bf16x2(x.z * inv, x.w * inv);
-      L = (m2 + __log2f(l)) * kLn2;
     }
-  }
-  if (write) {
-    reinterpret_cast<uint2*>(O + row * kHeadDim)[lane] = out;
-    if (lane == 0) lse[row] = L;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + 2 * i + (lane >> 4);
+      if (row >= rows) continue;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      float L = -INFINITY;
+      if (m2[i] != -INFINITY) {
+        if (!(l[i] >= kUnderflowSum) || !isfinite(l[i])) {
+          if (sub == 0) {
+            const int32_t k = atomicAdd(list, 1);
+            list[1 + k] = int32_t(row);
+          }
+          continue;  // the fallback kernel writes this row
+        }
+        const float inv = 1.f / l[i];
+        out = make_uint4(pack_bf16x2(a[i].x * inv, a[i].y * inv), pack_bf16x2(a[i].z * inv, a[i].w * inv),
+                         pack_bf16x2(b[i].x * inv, b[i].y * inv), pack_bf16x2(b[i].z * inv, b[i].w * inv));
+        L = (m2[i] + __log2f(l[i])) * kLn2;
+      }
+      reinterpret_cast<uint4*>(O + row * kHeadDim)[sub] = out;
+      if (sub == 0) lse[row] = L;
+    }
   }
 }
 
@@ -757,7 +790,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   launch_end("fwd_main", s);
   const int64_t rows = p.T * kQHeads;
   launch_begin("fwd_finalize", s);
-  k_fwd_finalize<<<unsigned((rows + 7) / 8), 256, 0, s>>>(
+  k_fwd_finalize<<<unsigned(device_sm_count() * 16), 256, 0, s>>>(
       p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o), lse, list);
   launch_end("fwd_finalize", s);
   launch_begin("fwd_fallback", s);
