@@ -73,6 +73,8 @@ SIGNATURES = {
     "msa_plan_workspace_bytes": ([_I64, _I32, ctypes.POINTER(_SZ)], _I32),
     "msa_build_plan": ([_P, _P, _I64, _I32, ctypes.POINTER(MsaPlanOptions), _P, _SZ, _P, _PLAN],
                        _I32),
+    "msa_build_plan_static": ([_P, _P, _I64, _I32, ctypes.POINTER(MsaPlanOptions), _P, _PLAN],
+                              _I32),
     "msa_forward_workspace_bytes": ([_PLAN, ctypes.POINTER(_SZ)], _I32),
     "msa_forward": ([_PLAN, _P, _P, _P, _F, _P, _P, _P, _SZ, _P], _I32),
     "msa_backward_workspace_bytes": ([_PLAN, ctypes.POINTER(_SZ)], _I32),
@@ -179,6 +181,24 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
                                 _ptr(workspace), workspace.numel(), _stream(stream),
                                 ctypes.byref(st)), "msa_build_plan")
     return Plan(st, workspace, q2k, doc_offsets)
+
+
+def msa_build_plan_static(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 16,
+                          stream=None, dq_accum: str = "f16") -> Plan:
+    """Like msa_build_plan, but the plan tables live in the library's own
+    static device array, so nothing is allocated.  For callers that cannot
+    allocate device memory; the plan is valid until the next call."""
+    if q2k.dim() != 3:
+        raise ValueError("q2k must be [4, T, 16]")
+    T = int(q2k.shape[1])
+    D = int(doc_offsets.numel()) - 1
+    _need(q2k, "q2k", torch.int32, (NUM_KV_HEADS, T, TOPK))
+    _need(doc_offsets, "doc_offsets", torch.int32, (D + 1,))
+    opts = MsaPlanOptions(super_block=super_block, dq_accum=DQ_ACCUM[dq_accum])
+    st = MsaPlanStruct()
+    _check(lib().msa_build_plan_static(_ptr(q2k), _ptr(doc_offsets), T, D, ctypes.byref(opts),
+                                       _stream(stream), ctypes.byref(st)), "msa_build_plan_static")
+    return Plan(st, None, q2k, doc_offsets)
 
 
 def forward_workspace_bytes(plan: Plan) -> int:

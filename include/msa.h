@@ -148,6 +148,27 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
                           int32_t num_docs, const msa_plan_options* opts, void* workspace,
                           size_t workspace_bytes, msa_stream_t stream, msa_plan* out);
 
+/*
+ * msa_build_plan with the plan tables in device memory owned by the library,
+ * for callers that cannot allocate device memory where they need a plan (a
+ * memory manager that forbids allocation at that point, a hook that is handed
+ * only the input buffers).  The pages have no counterpart of this call.
+ *   - The tables live in one static 16 MiB device array that every GPU which
+ *     loads the library keeps until the process exits; T and num_docs whose
+ *     msa_plan_workspace_bytes exceeds 16 MiB are rejected with
+ *     MSA_ERR_WORKSPACE (roughly T <= 16384 tokens; the exact bound depends on
+ *     the number of documents).
+ *   - The first call on a device looks the array up (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - Every call reuses the same array: the returned plan is valid until the
+ *     next msa_build_plan_static call on that device, and calls (or uses of
+ *     the plan) that overlap on the GPU race.  Nothing else is allocated.
+ * Arguments, validation and errors otherwise as msa_build_plan.
+ */
+msa_status msa_build_plan_static(const int32_t* q2k, const int32_t* doc_offsets, int64_t T,
+                                 int32_t num_docs, const msa_plan_options* opts,
+                                 msa_stream_t stream, msa_plan* out);
+
 /* Bytes of forward workspace for a plan (host only). */
 msa_status msa_forward_workspace_bytes(const msa_plan* plan, size_t* bytes);
 
