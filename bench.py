@@ -100,10 +100,34 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank
+def reduce_over_ranks(x: float, world: int, op: str = "max") -> float:
+    """Max (the slowest rank's time) or sum (work done by all ranks) of one
+    number over the ranks of the default process group; identity at N=1."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    red = torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM
+    torch.distributed.all_reduce(t, op=red)
+    return float(t.item())
+
+
+def aggregate(total_ms: float, steps: int, flop_step: float, tokens: int, world: int):
+    """Whole-job figures of a weak-scaling run: every rank processed its own
+    replica; the job took as long as its slowest rank.  Returns
+    (ms_per_step, TFLOP/s over all ranks, tokens/s over all ranks)."""
+    ms = reduce_over_ranks(total_ms, world, "max") / steps
+    flop = reduce_over_ranks(flop_step, world, "sum")
+    tok = reduce_over_ranks(tokens, world, "sum")
+    return ms, flop / (ms * 1e-3) / 1e12, tok / (ms * 1e-3)
+
+
 # ---------------------------------------------------------------- reference arm
-def cpu_sample(w, budget_s: float = 20.0):
+def cpu_sample(w, budget_s: float = 20.0, max_doc_tokens: int = 0):
     """Time the fp64 oracle's forward + backward on whole documents of the
-    workload (documents are independent, so each is a faithful sample)."""
+    workload (documents are independent, so each is a faithful sample).  With
+    ``max_doc_tokens`` each document is cut to that prefix, which is itself a
+    valid document (causal attention never looks past a query)."""
     import oracle
     offs = w.doc_offsets.numpy()
     lens = np.diff(offs)
@@ -114,6 +138,8 @@ def cpu_sample(w, budget_s: float = 20.0):
     used = []
     for d in order:
         s, e = int(offs[d]), int(offs[d + 1])
+        if max_doc_tokens > 0:
+            e = min(e, s + max_doc_tokens)
         sub = inputs.Workload(
             name="doc", q=w.q[s:e], k=w.k[s:e], v=w.v[s:e], do=w.do[s:e],
             q2k=w.q2k[:, s:e].contiguous(),
@@ -133,8 +159,9 @@ def cpu_sample(w, budget_s: float = 20.0):
     return {
         "flops": flops, "seconds": spent, "tokens": int(sum(used)), "docs": len(used),
         "pairs": pairs_total, "cores": oracle.threads(),
-        "sample": f"{len(used)} whole document(s) ({sum(used)} tokens, lengths {used}) of the "
-                  f"packed T=16384 row: oracle forward + backward in fp64",
+        "sample": f"{len(used)} {'document prefix(es)' if max_doc_tokens > 0 else 'whole document(s)'}"
+                  f" ({sum(used)} tokens, lengths {used}) of the packed T=16384 row: oracle "
+                  f"forward + backward in fp64",
     }
 
 
@@ -142,12 +169,12 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = inputs.config(WORKLOAD)
-    budget = max(3.0, 30.0 / max(1, args.steps + args.warmup))
+    budget = args.sample_seconds or max(3.0, 30.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_sample(w, budget)
+        cpu_sample(w, budget, args.sample_max_tokens)
     times, flops, last = [], 0.0, None
     for _ in range(args.steps):
-        last = cpu_sample(w, budget)
+        last = cpu_sample(w, budget, args.sample_max_tokens)
         times.append(last["seconds"])
         flops += last["flops"]
     total = sum(times)
@@ -241,15 +268,8 @@ def run_gpu(args, rank, world):
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
     step_ms = [a + b + c for a, b, c in zip(plan_ms, fwd_ms, bwd_ms)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
     flop_step = flop_fwd + flop_bwd
-    value = world * flop_step / (ms_per_step * 1e-3) / 1e12
-    tok_s = world * T / (ms_per_step * 1e-3)
+    ms_per_step, value, tok_s = aggregate(sum(step_ms), args.steps, flop_step, T, world)
 
     # ---- end to end through the public API with host buffers
     pin = lambda x: x.pin_memory()  # noqa: E731
@@ -285,11 +305,8 @@ def run_gpu(args, rank, world):
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = ea.elapsed_time(eb) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flop_step / (e2e_ms * 1e-3) / 1e12
+    _, e2e_value, _ = aggregate(e2e_ms, 1, flop_step, T, world)
+    e2e_ms = reduce_over_ranks(e2e_ms, world, "max")
     if rank != 0:
         return
 
@@ -348,6 +365,10 @@ def main():
     ap.add_argument("--super-block", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--sample-seconds", type=float, default=0.0,
+                    help="reference arm: CPU seconds per step (default: about 30 s per run)")
+    ap.add_argument("--sample-max-tokens", type=int, default=0,
+                    help="reference arm: cut sampled documents to this prefix (0 = whole)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
