@@ -100,6 +100,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- recorded DRAM traffic
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu record in
+    profiles/, or None when there is none for this workload or the kernel's
+    sources changed since the counters were taken (hash mismatch)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("source_files", []):
+        p = os.path.join(ROOT, src)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec.get("source_sha256_16"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
 # ---------------------------------------------------------------- multi-rank
 def reduce_over_ranks(x: float, world: int, op: str = "max") -> float:
     """Max (the slowest rank's time) or sum (work done by all ranks) of one
@@ -317,13 +342,7 @@ def run_gpu(args, rank, world):
     per_launch_ms = kern[dom]["ms_per_step"] * args.steps / kern[dom]["launches"]
     achieved = dom_flop / (per_launch_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    traffic_path = os.path.join(ROOT, "profiles", f"{dom}_traffic.json")
-    traffic = None
-    if os.path.exists(traffic_path):
-        with open(traffic_path) as f:
-            tj = json.load(f)
-        if tj.get("workload") == w.name:
-            traffic = tj.get("bytes_per_launch")
+    traffic = recorded_traffic(dom, w.name)
 
     cpu = cpu_sample(w, budget_s=20.0) if not args.no_cpu_baseline else None
     line = {

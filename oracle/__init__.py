@@ -9,6 +9,11 @@ shares no code with it.
 Inputs are CPU torch tensors (bf16 tensors are widened exactly to fp64 here),
 uint16 numpy arrays holding bf16 bit patterns, or float64 numpy arrays (used
 unrounded, e.g. by finite-difference tests).  Outputs are float64 arrays.
+
+``Problem(..., bf16_input=True)`` uses a second build of the same C source that
+reads the bf16 bit patterns directly and widens each element where it is read
+(no fp64 copy of the inputs: for problems of 10^5 tokens and more); it returns
+bit-identical results.
 """
 from __future__ import annotations
 
@@ -22,8 +27,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "msa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libmsa_oracle.so")
+_LIB16_PATH = os.path.join(_HERE, "libmsa_oracle_bf16in.so")
 _lock = threading.Lock()
 _lib = None
+_lib16 = None
 
 OR_OK, OR_BAD_ARGS, OR_BAD_Q2K, OR_CAPACITY = 0, 1, 2, 3
 
@@ -33,22 +40,34 @@ class OracleError(RuntimeError):
 
 
 def build(force: bool = False, extra_flags: tuple[str, ...] = (), out: str | None = None) -> str:
-    """Compile msa_oracle.c with gcc (-O2, OpenMP).  Returns the .so path."""
-    out = out or _LIB_PATH
-    if (not force and os.path.exists(out)
-            and os.path.getmtime(out) >= os.path.getmtime(_SRC) and not extra_flags):
+    """Compile msa_oracle.c with gcc (-O2, OpenMP), the fp64-input library and
+    the bf16-input one.  Returns the fp64-input .so path (or ``out``)."""
+    if out is not None or extra_flags:
+        _compile(out or _LIB_PATH, extra_flags, force=True)
+        return out or _LIB_PATH
+    _compile(_LIB16_PATH, ("-DORACLE_BF16_INPUT",), force)
+    return _compile(_LIB_PATH, (), force)
+
+
+def _compile(out: str, flags, force: bool) -> str:
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
         return out
-    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c99", *extra_flags,
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c99", *flags,
            "-o", out, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     return out
 
 
-def _load(path: str | None = None):
-    global _lib
+def _load(path: str | None = None, bf16_input: bool = False):
+    global _lib, _lib16
     if path is not None:
         return _bind(ctypes.CDLL(path))
     with _lock:
+        if bf16_input:
+            if _lib16 is None:
+                build()
+                _lib16 = _bind(ctypes.CDLL(_LIB16_PATH))
+            return _lib16
         if _lib is None:
             _lib = _bind(ctypes.CDLL(build()))
     return _lib
@@ -90,6 +109,18 @@ def _f64(x) -> np.ndarray:
     return np.ascontiguousarray(x.detach().cpu().to(torch.float64).numpy())
 
 
+def _bf16_bits(x) -> np.ndarray:
+    """The bf16 bit patterns of a bf16 tensor (or a uint16 array) as uint16."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("expected uint16 bf16 bit patterns")
+        return np.ascontiguousarray(x)
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("bf16_input needs bfloat16 tensors")
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def _i32(x) -> np.ndarray:
     if not isinstance(x, np.ndarray):
         x = x.detach().cpu().numpy()
@@ -108,21 +139,24 @@ def _check(rc: int, what: str):
 class Problem:
     """Holds the converted inputs of one MSA problem for repeated oracle calls."""
 
-    def __init__(self, q, k, v, q2k, doc_offsets, scale, do=None, lib_path: str | None = None):
-        self.q = _f64(q)
-        self.k = _f64(k)
-        self.v = _f64(v)
-        self.do = None if do is None else _f64(do)
+    def __init__(self, q, k, v, q2k, doc_offsets, scale, do=None, lib_path: str | None = None,
+                 bf16_input: bool = False):
+        conv = _bf16_bits if bf16_input else _f64
+        self.q = conv(q)
+        self.k = conv(k)
+        self.v = conv(v)
+        self.do = None if do is None else conv(do)
         self.q2k = _i32(q2k)
         self.offs = _i32(doc_offsets)
         self.T = int(self.q.shape[0])
         self.D = int(self.offs.size - 1)
         self.scale = float(scale)
-        self.lib = _load(lib_path)
+        self.lib = _load(lib_path, bf16_input)
 
     @classmethod
-    def from_workload(cls, w, lib_path: str | None = None):
-        return cls(w.q, w.k, w.v, w.q2k, w.doc_offsets, w.scale, do=w.do, lib_path=lib_path)
+    def from_workload(cls, w, lib_path: str | None = None, bf16_input: bool = False):
+        return cls(w.q, w.k, w.v, w.q2k, w.doc_offsets, w.scale, do=w.do, lib_path=lib_path,
+                   bf16_input=bf16_input)
 
     def forward(self, toks=None):
         """(O [n,64,128], LSE [n,64]) for the listed tokens (all if None)."""

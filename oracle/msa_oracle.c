@@ -31,6 +31,10 @@
  * Inputs: fp64 arrays.  The Python wrapper widens the bf16 tensors of a
  * problem exactly (bf16 -> fp32 -> fp64), so the oracle sees the same values
  * the GPU path reads; finite-difference tests pass unrounded fp64 values.
+ * Built with -DORACLE_BF16_INPUT the same source takes Q, K, V, dO as the
+ * bf16 bit patterns themselves and widens each element exactly where it is
+ * read, so large problems need no fp64 copy; every arithmetic step is the
+ * same, so both builds return bit-identical results on bf16 values.
  * All arithmetic is fp64.  Parallelism is OpenMP over independent
  * rows / buckets only; there is no blocking or fusion beyond the definitions.
  */
@@ -50,6 +54,20 @@
 #define TOPK 16  /* q2k slots */
 
 enum { OR_OK = 0, OR_BAD_ARGS = 1, OR_BAD_Q2K = 2, OR_CAPACITY = 3 };
+
+/* Element type of Q, K, V, dO and its exact widening to fp64. */
+#ifdef ORACLE_BF16_INPUT
+typedef uint16_t elem_t;
+static inline double ld(const elem_t* p, int64_t i) {
+  uint32_t u = (uint32_t)p[i] << 16; /* bf16 is the top half of an fp32 */
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+#else
+typedef double elem_t;
+static inline double ld(const elem_t* p, int64_t i) { return p[i]; }
+#endif
 
 /* Document offsets: offs[0] = 0, strictly increasing, offs[D] = T. */
 static int check_offsets(const int32_t* offs, int32_t D, int64_t T) {
@@ -115,19 +133,19 @@ static int check_q2k(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t
 }
 
 /* scale * <Q[t,h,:], K[j,g,:]> */
-static double score(const double* Q, const double* K, int64_t t, int h, int64_t j, int g,
+static double score(const elem_t* Q, const elem_t* K, int64_t t, int h, int64_t j, int g,
                     double scale) {
-  const double* q = Q + ((int64_t)t * NQH + h) * HD;
-  const double* k = K + ((int64_t)j * NKV + g) * HD;
+  const elem_t* q = Q + ((int64_t)t * NQH + h) * HD;
+  const elem_t* k = K + ((int64_t)j * NKV + g) * HD;
   double acc = 0.0;
-  for (int c = 0; c < HD; ++c) acc += q[c] * k[c];
+  for (int c = 0; c < HD; ++c) acc += ld(q, c) * ld(k, c);
   return scale * acc;
 }
 
 /* Forward of one query token t for the 16 heads of index head g:
  * LSE[h] = ln sum_j exp(s_j), P_j = exp(s_j - LSE), O[h] = sum_j P_j V[j,g].
  * o: [16][128], lse: [16].  s: scratch of nkeys doubles. */
-static void row_forward(const double* Q, const double* K, const double* V, int64_t t, int g,
+static void row_forward(const elem_t* Q, const elem_t* K, const elem_t* V, int64_t t, int g,
                         const int64_t* keys, int64_t nkeys, double scale, double* s, double* o,
                         double* lse) {
   for (int hh = 0; hh < HPG; ++hh) {
@@ -149,8 +167,8 @@ static void row_forward(const double* Q, const double* K, const double* V, int64
     lse[hh] = L;
     for (int64_t i = 0; i < nkeys; ++i) {
       double pr = exp(s[i] - L);
-      const double* vr = V + ((int64_t)keys[i] * NKV + g) * HD;
-      for (int c = 0; c < HD; ++c) oh[c] += pr * vr[c];
+      const elem_t* vr = V + ((int64_t)keys[i] * NKV + g) * HD;
+      for (int c = 0; c < HD; ++c) oh[c] += pr * ld(vr, c);
     }
   }
 }
@@ -160,7 +178,7 @@ static void row_forward(const double* Q, const double* K, const double* V, int64
  * toks == NULL means every token 0..T-1 (ntoks must equal T).
  * O: [ntoks][64][128], LSE: [ntoks][64].
  */
-int oracle_forward(const double* Q, const double* K, const double* V, const int32_t* q2k,
+int oracle_forward(const elem_t* Q, const elem_t* K, const elem_t* V, const int32_t* q2k,
                    int64_t T, const int32_t* offs, int32_t D, double scale, const int64_t* toks,
                    int64_t ntoks, double* O, double* LSE) {
   if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
@@ -201,7 +219,7 @@ int oracle_forward(const double* Q, const double* K, const double* V, const int3
  * O, LSE and delta are recomputed exactly here.  dQ: [ntoks][64][128].
  * If DELTA is not NULL it receives delta [ntoks][64].
  */
-int oracle_dq(const double* Q, const double* K, const double* V, const double* dO,
+int oracle_dq(const elem_t* Q, const elem_t* K, const elem_t* V, const elem_t* dO,
               const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, double scale,
               const int64_t* toks, int64_t ntoks, double* dQ, double* DELTA) {
   if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
@@ -224,21 +242,21 @@ int oracle_dq(const double* Q, const double* K, const double* V, const double* d
         row_forward(Q, K, V, t, g, keys, nk, scale, s, o, lse);
         for (int hh = 0; hh < HPG; ++hh) {
           int h = g * HPG + hh;
-          const double* dor = dO + ((int64_t)t * NQH + h) * HD;
+          const elem_t* dor = dO + ((int64_t)t * NQH + h) * HD;
           double* dq = dQ + (i * NQH + h) * HD;
           double delta = 0.0;
-          for (int c = 0; c < HD; ++c) delta += dor[c] * o[hh * HD + c];
+          for (int c = 0; c < HD; ++c) delta += ld(dor, c) * o[hh * HD + c];
           if (DELTA) DELTA[i * NQH + h] = delta;
           for (int c = 0; c < HD; ++c) dq[c] = 0.0;
           for (int64_t kk = 0; kk < nk; ++kk) {
             int64_t j = keys[kk];
             double pr = exp(score(Q, K, t, h, j, g, scale) - lse[hh]);
-            const double* vr = V + (j * NKV + g) * HD;
-            const double* kr = K + (j * NKV + g) * HD;
+            const elem_t* vr = V + (j * NKV + g) * HD;
+            const elem_t* kr = K + (j * NKV + g) * HD;
             double dp = 0.0;
-            for (int c = 0; c < HD; ++c) dp += dor[c] * vr[c];
+            for (int c = 0; c < HD; ++c) dp += ld(dor, c) * ld(vr, c);
             double ds = pr * (dp - delta);
-            for (int c = 0; c < HD; ++c) dq[c] += scale * ds * kr[c];
+            for (int c = 0; c < HD; ++c) dq[c] += scale * ds * ld(kr, c);
           }
         }
       }
@@ -257,8 +275,8 @@ int oracle_dq(const double* Q, const double* K, const double* V, const double* d
  *   dV_j += P_tj dO_t,   dK_j += scale * dS_tj Q_t.
  * dK, dV: [nblk_req][128][128] (rows past the document end stay zero).
  */
-int oracle_dkv_blocks(const double* Q, const double* K, const double* V,
-                      const double* dO, const int32_t* q2k, int64_t T, const int32_t* offs,
+int oracle_dkv_blocks(const elem_t* Q, const elem_t* K, const elem_t* V,
+                      const elem_t* dO, const int32_t* q2k, int64_t T, const int32_t* offs,
                       int32_t D, double scale, const int64_t* blocks, int64_t nblk_req,
                       double* dK, double* dV) {
   if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
@@ -304,20 +322,20 @@ int oracle_dkv_blocks(const double* Q, const double* K, const double* V,
         row_forward(Q, K, V, t, g, keys, nk, scale, s, o, lse);
         for (int hh = 0; hh < HPG; ++hh) {
           int h = g * HPG + hh;
-          const double* dor = dO + (t * NQH + h) * HD;
-          const double* qr = Q + (t * NQH + h) * HD;
+          const elem_t* dor = dO + (t * NQH + h) * HD;
+          const elem_t* qr = Q + (t * NQH + h) * HD;
           double delta = 0.0;
-          for (int c = 0; c < HD; ++c) delta += dor[c] * o[hh * HD + c];
+          for (int c = 0; c < HD; ++c) delta += ld(dor, c) * o[hh * HD + c];
           for (int64_t r = 0; r < klen && k0 + r <= t; ++r) {
             int64_t j = k0 + r;
             double pr = exp(score(Q, K, t, h, j, g, scale) - lse[hh]);
-            const double* vr = V + (j * NKV + g) * HD;
+            const elem_t* vr = V + (j * NKV + g) * HD;
             double dp = 0.0;
-            for (int c = 0; c < HD; ++c) dp += dor[c] * vr[c];
+            for (int c = 0; c < HD; ++c) dp += ld(dor, c) * ld(vr, c);
             double ds = pr * (dp - delta);
             for (int c = 0; c < HD; ++c) {
-              pv[r * HD + c] += pr * dor[c];
-              pk[r * HD + c] += scale * ds * qr[c];
+              pv[r * HD + c] += pr * ld(dor, c);
+              pk[r * HD + c] += scale * ds * ld(qr, c);
             }
           }
         }
@@ -343,7 +361,7 @@ int oracle_dkv_blocks(const double* Q, const double* K, const double* V,
  * oracle_dq over all tokens; dK/dV from oracle_dkv_blocks over every (index
  * head, key block) of every document, scattered back to token rows.
  */
-int oracle_backward(const double* Q, const double* K, const double* V, const double* dO,
+int oracle_backward(const elem_t* Q, const elem_t* K, const elem_t* V, const elem_t* dO,
                     const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D, double scale,
                     double* dQ, double* dK, double* dV) {
   int rc = oracle_dq(Q, K, V, dO, q2k, T, offs, D, scale, NULL, T, dQ, NULL);

@@ -286,6 +286,23 @@ def test_dkv_blocks_match_full_backward(oracle_mod):
     assert (bk[1, 140:] == 0).all()
 
 
+def test_bf16_input_build_is_bit_identical(oracle_mod):
+    """The bf16-input build (inputs read as bf16 bits and widened where they
+    are read) does the same fp64 arithmetic: results equal bit for bit."""
+    w = sparse_case([300, 1, 140], seed=23, p_empty=0.1, p_future=0.1)
+    A = problem(oracle_mod, w)
+    B = oracle_mod.Problem.from_workload(w, bf16_input=True)
+    assert B.q.dtype == np.uint16 and B.lib is not A.lib
+    toks = [0, 5, 127, 128, 299, 300, 301, 440]
+    for a, b in zip(A.forward(toks), B.forward(toks)):
+        assert np.array_equal(a, b)
+    for a, b in zip(A.dq(toks, with_delta=True), B.dq(toks, with_delta=True)):
+        assert np.array_equal(a, b)
+    blocks = [(0, 0), (2, 256), (3, 301)]
+    for a, b in zip(A.dkv_blocks(blocks), B.dkv_blocks(blocks)):
+        assert np.array_equal(a, b)
+
+
 def test_bad_q2k_rejected(oracle_mod):
     w = inputs.custom([200], seed=22)
     q2k = w.q2k.numpy().copy()
