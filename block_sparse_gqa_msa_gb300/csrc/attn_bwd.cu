@@ -117,7 +117,7 @@ constexpr uint32_t kTmP = 0, kTmDST = 128, kTmDQ = 128;
 __device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full, dk_done, dv_done,
+  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full[2], dk_done, dv_done,
       dq_full, dq_free, dkv_free, fin;
 };
 
@@ -153,6 +153,113 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
 }
 
+// MMA issuer of k_bwd_main (one thread).  A function of its own so its few
+// live values stay in registers whatever the compute roles need.
+//
+// Per task t (waits in brackets):
+//   [dq_free(t-1)] dP^T(t)  [pds_0] dK, dV k-steps of q-rows 0-63
+//   [pds_1] dK, dV k-steps of q-rows 64-127  [dk_done] dQ^T(t)  [dv_done] S^T(t+1)
+// so the GEMMs of the first half overlap the softmax of the second.
+__device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t sbase,
+                                          const int4* tasks, int64_t my_n, int chunk,
+                                          volatile int* abort_flag) {
+  constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
+  constexpr uint32_t idTS = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
+  constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T
+  auto wait = [&](uint64_t& bar, uint32_t ph) {
+    const bool ok = mbar_wait(smem_u32(&bar), ph, abort_flag);
+    tc_fence_after();
+    return ok;
+  };
+  // Descriptors are built once; a k-step only adds a constant to the
+  // start-address field (addresses stay below 256 KB, so the 14-bit field
+  // never carries).  Rebuilding a descriptor per MMA costs more issue time
+  // than a 128x128x16 MMA takes to run.
+  const uint64_t kK = sdesc_sw128(sbase + kSmK, 16u, 1024u);       // K, K-major
+  const uint64_t kV = sdesc_sw128(sbase + kSmV, 16u, 1024u);       // V, K-major
+  const uint64_t mK = sdesc_sw128(sbase + kSmK, 16384u, 1024u);    // K, MN-major
+  const uint64_t mDS = sdesc_sw128(sbase + kSmDS, 16384u, 1024u);  // dS, MN-major
+  const uint64_t kQ0 = sdesc_sw128(sbase + kSmQ, 16u, 1024u);
+  const uint64_t kDO0 = sdesc_sw128(sbase + kSmDO, 16u, 1024u);
+  const uint64_t mQ0 = sdesc_sw128(sbase + kSmQ, 16384u, 1024u);
+  const uint64_t mDO0 = sdesc_sw128(sbase + kSmDO, 16384u, 1024u);
+  constexpr uint64_t kStage = kTileBytes >> 4;
+  // start-address steps (16-byte units): K-major k-step, MN-major k-step
+  auto kstep = [](int kk) { return uint64_t((kk >> 2) * 1024 + (kk & 3) * 2); };
+  auto mstep = [](int kk) { return uint64_t(kk) * 128u; };
+  auto issue_S = [&](int64_t t) {
+    const uint64_t b = kQ0 + uint64_t(t & 1) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(tmem + kTmS, kK + kstep(kk), b + kstep(kk), idKK, kk > 0);
+  };
+  auto issue_dP = [&](int64_t t) {
+    const uint64_t b = kDO0 + uint64_t(t & 1) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(tmem + kTmDP, kV + kstep(kk), b + kstep(kk), idKK, kk > 0);
+    umma_commit(smem_u32(&bars.sdp_full));
+  };
+  // dK += dS^T Q and dV += P^T dO over the four k-steps of one half of the q-rows
+  auto issue_dkdv = [&](int64_t t, int h, uint32_t acc0) {
+    const uint64_t bq = mQ0 + uint64_t(t & 1) * kStage;
+    const uint64_t bo = mDO0 + uint64_t(t & 1) * kStage;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      umma_ts(tmem + kTmDK, tmem + kTmDST + ts_col(4 * h + j), bq + mstep(4 * h + j), idTS,
+              j > 0 ? 1u : acc0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      umma_ts(tmem + kTmDV, tmem + kTmP + ts_col(4 * h + j), bo + mstep(4 * h + j), idTS,
+              j > 0 ? 1u : acc0);
+  };
+  int64_t kv_loads = 1, seg_done = 0;
+  bool first_in_seg = true;
+  int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
+  int next_kv = task_rec(tasks, 1, my_n, chunk).w;
+  bool ok = wait(bars.kv_full, 0) && wait(bars.qdo_full[0], 0);
+  if (ok) issue_S(0);
+  for (int64_t it = 0; ok && it < my_n; ++it) {
+    const uint32_t ph = uint32_t(it & 1);
+    const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;  // used next iteration
+    // dP^T(it) overwrites dQ^T(it-1): the reducers must have read it.
+    if (it >= 1 && !wait(bars.dq_free, ph ^ 1u)) break;
+    issue_dP(it);
+    if (!wait(bars.pds_full[0], ph)) break;
+    if (first_in_seg && seg_done > 0 && !wait(bars.dkv_free, uint32_t((seg_done - 1) & 1)))
+      break;
+    issue_dkdv(it, 0, first_in_seg ? 0u : 1u);
+    if (!wait(bars.pds_full[1], ph)) break;
+    issue_dkdv(it, 1, 1u);
+    umma_commit(smem_u32(&bars.dk_done));
+    umma_commit(smem_u32(&bars.dv_done));
+    // dQ^T is written over dS^T: dK must have read it.
+    if (!wait(bars.dk_done, ph)) break;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(tmem + kTmDQ, mK + mstep(kk), mDS + mstep(kk), idMM, kk > 0);
+    umma_commit(smem_u32(&bars.dq_full));
+    first_in_seg = false;
+    if (it + 1 < my_n) {
+      if (next_kv != cur_kv) {
+        ++seg_done;
+        umma_commit(smem_u32(&bars.kv_empty));
+        if (!wait(bars.kv_full, uint32_t(kv_loads & 1))) break;
+        ++kv_loads;
+        cur_kv = next_kv;
+        first_in_seg = true;
+      }
+      // S^T(it+1) overwrites P^T(it): dV(it) must have read it.
+      if (!wait(bars.dv_done, ph)) break;
+      if (!wait(bars.qdo_full[(it + 1) & 1], uint32_t(((it + 1) >> 1) & 1))) break;
+      issue_S(it + 1);
+    }
+    next_kv = next2_kv;
+  }
+  umma_commit(smem_u32(&bars.fin));
+  mbar_wait_drain(smem_u32(&bars.fin), 0);
+}
+
 // Warp roles (448 threads):
 //   0      TMA producer: K/V per block run, Q/dO per task (two stages)
 //   1      MMA issuer, TMEM owner
@@ -167,7 +274,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ BwdBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
-  __shared__ __align__(16) float s_lse2[128];
+  __shared__ __align__(16) float s_nlse2[128];  // -LSE * log2(e)
   __shared__ __align__(16) float s_delta[128];
   __shared__ __align__(16) int8_t s_jlim[128];
   __shared__ int s_wfull[4];  // per lane quadrant: every column sees all 128 keys
@@ -188,7 +295,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bars.qdo_empty[i]), 1);
     }
     mbar_init(smem_u32(&bars.sdp_full), 1);
-    mbar_init(smem_u32(&bars.pds_full), 256);
+    mbar_init(smem_u32(&bars.pds_full[0]), 128);
+    mbar_init(smem_u32(&bars.pds_full[1]), 128);
     mbar_init(smem_u32(&bars.dk_done), 1);
     mbar_init(smem_u32(&bars.dv_done), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
@@ -277,151 +385,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) {
-      constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t idTS = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
-      constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T
-      int64_t kv_loads = 0, seg_done = 0;
-      bool first_in_seg = true;
-      auto issue_S = [&](int64_t it) -> bool {
-        const int st = int(it & 1);
-        if (!mbar_wait(smem_u32(&bars.qdo_full[st]), uint32_t((it >> 1) & 1), abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t sq = sbase + kSmQ + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmS, desc_kmajor(sbase + kSmK, kk), desc_kmajor(sq, kk), idKK, kk > 0);
-        return true;
-      };
-      int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
-      int next_kv = task_rec(tasks, 1, my_n, chunk).w;
-      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abort_flag);
-      kv_loads = 1;
-      ok = ok && issue_S(0);
-      for (int64_t it = 0; ok && it < my_n; ++it) {
-        const int st = int(it & 1);
-        const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;  // used next iteration
-        // dP^T(it) overwrites dQ^T(it-1): the reducers must have read it.
-        if (it >= 1 && !mbar_wait(smem_u32(&bars.dq_free), uint32_t((it - 1) & 1), abort_flag))
-          break;
-        tc_fence_after();
-        const uint32_t sdo = sbase + kSmDO + st * kTileBytes;
-        const uint32_t sq = sbase + kSmQ + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDP, desc_kmajor(sbase + kSmV, kk), desc_kmajor(sdo, kk), idKK,
-                  kk > 0);
-        umma_commit(smem_u32(&bars.sdp_full));
-        if (!mbar_wait(smem_u32(&bars.pds_full), uint32_t(it & 1), abort_flag)) break;
-        if (first_in_seg && seg_done > 0 &&
-            !mbar_wait(smem_u32(&bars.dkv_free), uint32_t((seg_done - 1) & 1), abort_flag))
-          break;
-        tc_fence_after();
-        const uint32_t acc0 = first_in_seg ? 0u : 1u;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kTmDK, tmem + kTmDST + ts_col(kk), desc_mnmajor(sq, kk), idTS,
-                  kk > 0 ? 1u : acc0);
-        umma_commit(smem_u32(&bars.dk_done));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + kTmDV, tmem + kTmP + ts_col(kk), desc_mnmajor(sdo, kk), idTS,
-                  kk > 0 ? 1u : acc0);
-        umma_commit(smem_u32(&bars.dv_done));
-        // dQ^T is written over dS^T: dK must have read it (dV keeps the pipe busy).
-        if (!mbar_wait(smem_u32(&bars.dk_done), uint32_t(it & 1), abort_flag)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + kTmDQ, desc_mnmajor(sbase + kSmK, kk), desc_mnmajor(sbase + kSmDS, kk),
-                  idMM, kk > 0);
-        umma_commit(smem_u32(&bars.dq_full));
-        first_in_seg = false;
-        if (it + 1 < my_n) {
-          if (next_kv != cur_kv) {
-            ++seg_done;
-            umma_commit(smem_u32(&bars.kv_empty));
-            if (!mbar_wait(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) break;
-            ++kv_loads;
-            cur_kv = next_kv;
-            first_in_seg = true;
-          }
-          // S^T(it+1) overwrites P^T(it): dV(it) must have read it (dQ^T keeps the pipe busy).
-          if (!mbar_wait(smem_u32(&bars.dv_done), uint32_t(it & 1), abort_flag)) break;
-          if (!issue_S(it + 1)) break;
-        }
-        next_kv = next2_kv;
-      }
-      umma_commit(smem_u32(&bars.fin));
-      mbar_wait_drain(smem_u32(&bars.fin), 0);
-    }
+    if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, my_n, chunk, abort_flag);
   } else if (warp < 10) {
     // ---------------- compute: P^T, dS^T (thread = key; half = block of 64 q-rows)
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // key within the block = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    // One 16-column sub-chunk (q-rows cb .. cb+15, cb = 64 half + 16 sc).
+    // One 16-column sub-chunk (q-rows cb .. cb+15, cb = 64 half + 16 sc), in
+    // fp32 pairs:  P = 2^(S^T c2 - LSE log2 e),  dS = P (dP^T - delta).
     auto sub_chunk = [&](int sc, const uint32_t (&sv)[16], const uint32_t (&dv)[16], bool full) {
       const int cb = half * 64 + sc * 16;
-      const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + cb);
-      const float4* d4 = reinterpret_cast<const float4*>(s_delta + cb);
+      const uint4* l4 = reinterpret_cast<const uint4*>(s_nlse2 + cb);
+      const uint4* d4 = reinterpret_cast<const uint4*>(s_delta + cb);
       const uint4 jw = *reinterpret_cast<const uint4*>(s_jlim + cb);
       const uint32_t jwa[4] = {jw.x, jw.y, jw.z, jw.w};
-      float lse[16], dl[16];
+      uint64_t nl[8], dl[8];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 x = l4[q4], y = d4[q4];
-        lse[4 * q4] = x.x; lse[4 * q4 + 1] = x.y; lse[4 * q4 + 2] = x.z; lse[4 * q4 + 3] = x.w;
-        dl[4 * q4] = y.x; dl[4 * q4 + 1] = y.y; dl[4 * q4 + 2] = y.z; dl[4 * q4 + 3] = y.w;
+        const uint4 x = l4[q4], y = d4[q4];
+        nl[2 * q4] = f2_pack(x.x, x.y);
+        nl[2 * q4 + 1] = f2_pack(x.z, x.w);
+        dl[2 * q4] = f2_pack(y.x, y.y);
+        dl[2 * q4 + 1] = f2_pack(y.z, y.w);
       }
+      const uint64_t cc = f2_pack(__float_as_uint(prm.c2), __float_as_uint(prm.c2));
       uint32_t pp[8], pd[8];
-      if (full) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -lse[j]));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -lse[j + 1]));
-          pp[j >> 1] = pack_bf16x2(p0, p1);
-          pd[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[j]) - dl[j]),
-                                   p1 * (__uint_as_float(dv[j + 1]) - dl[j + 1]));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
+      for (int jp = 0; jp < 8; ++jp) {
+        const uint64_t x2 = f2_fma(f2_pack(sv[2 * jp], sv[2 * jp + 1]), cc, nl[jp]);
+        float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
+        if (!full) {  // keys after the column's query (diagonal block) get P = 0
+          const int j = 2 * jp;
           const int jl0 = int(int8_t((jwa[j >> 2] >> (8 * (j & 3))) & 0xFF));
           const int jl1 = int(int8_t((jwa[j >> 2] >> (8 * ((j + 1) & 3))) & 0xFF));
-          const float p0 =
-              r <= jl0 ? fast_exp2(fmaf(__uint_as_float(sv[j]), prm.c2, -lse[j])) : 0.f;
-          const float p1 =
-              r <= jl1 ? fast_exp2(fmaf(__uint_as_float(sv[j + 1]), prm.c2, -lse[j + 1])) : 0.f;
-          pp[j >> 1] = pack_bf16x2(p0, p1);
-          pd[j >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[j]) - dl[j]),
-                                   p1 * (__uint_as_float(dv[j + 1]) - dl[j + 1]));
+          p0 = r <= jl0 ? p0 : 0.f;
+          p1 = r <= jl1 ? p1 : 0.f;
         }
+        const uint64_t p2 = f2_pack(__float_as_uint(p0), __float_as_uint(p1));
+        const uint64_t ds = f2_mul(p2, f2_sub(f2_pack(dv[2 * jp], dv[2 * jp + 1]), dl[jp]));
+        pp[jp] = pack_bf16x2(p0, p1);
+        pd[jp] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
       }
-      tmem_st8(tmem + lane_base + kTmP + half * 64 + sc * 8, pp);
-      tmem_st8(tmem + lane_base + kTmDST + half * 64 + sc * 8, pd);
+      tmem_st8_nc(tmem + lane_base + kTmP + half * 64 + sc * 8, pp);
+      tmem_st8_nc(tmem + lane_base + kTmDST + half * 64 + sc * 8, pd);
       // dS (B operand of dQ^T, MN-major): tile row = key r, cols = q-rows
       const uint32_t rowb = sbase + kSmDS + half * 16384 + r * 128;
       const uint32_t c0 = uint32_t((2 * sc) ^ (r & 7)) * 16;
       const uint32_t c1 = uint32_t((2 * sc + 1) ^ (r & 7)) * 16;
-      st_shared_v4(rowb + c0, pd[0], pd[1], pd[2], pd[3]);
-      st_shared_v4(rowb + c1, pd[4], pd[5], pd[6], pd[7]);
+      st_shared_v4_nc(rowb + c0, pd[0], pd[1], pd[2], pd[3]);
+      st_shared_v4_nc(rowb + c1, pd[4], pd[5], pd[6], pd[7]);
     };
     // Column scalars of task it+1 are loaded while task it is computed, in
     // two steps so no load result is consumed right after it is issued: the
     // column's token at the top of task it, its LSE / delta mid-way.
     const int qi = r >> 4, hh = r & 15;
     int4 rec1 = task_rec(tasks, 1, my_n, chunk);
-    float cl2 = 0.f, cdl = 0.f;  // current task's column values
+    // (raw LSE: scaling it where it is loaded would wait for the load)
+    float clse = 0.f, cdl = 0.f;  // current task's column values
     int cjl = -1;
     if (half == 0 && my_n > 0) {
       const TaskView tv = decode_task(task_rec(tasks, 0, my_n, chunk));
       const int32_t tok = task_token(p.col, tv, qi);
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
       cjl = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
-      cl2 = prm.lse[grow] * kLog2e;
+      clse = prm.lse[grow];
       cdl = prm.delta[grow];
     }
     for (int64_t it = 0; it < my_n; ++it) {
@@ -430,7 +458,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (half == 0 && it + 1 < my_n) ntok = task_token(p.col, decode_task(rec1), qi);
       named_bar_sync(1, 256);  // previous task's columns fully consumed
       if (half == 0) {
-        s_lse2[r] = cl2;
+        s_nlse2[r] = -clse * kLog2e;
         s_delta[r] = cdl;
         s_jlim[r] = int8_t(cjl);
         const bool wf = __all_sync(0xffffffffu, cjl == kBlock - 1);
@@ -460,7 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const TaskView tn = decode_task(rec1);
             const int64_t grow = int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh;
             cjl = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
-            cl2 = prm.lse[grow] * kLog2e;
+            clse = prm.lse[grow];
             cdl = prm.delta[grow];
           }
         }
@@ -470,7 +498,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bars.pds_full));
+      mbar_arrive(smem_u32(&bars.pds_full[half]));
       rec1 = rec2;
     }
   } else {
@@ -539,8 +567,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         named_bar_sync(2, 128);
         if (issuer) {
           for (int qi = 0; qi < tv.nq; ++qi)
-            tma_reduce_add_2d(&mapDQ, stage_base + qi * 4096, 0,
-                              tok[qi] * kQHeads + tv.g * kHeadsPerGroup);
+            for (unsigned h0 = 0; h0 < unsigned(kHeadsPerGroup); h0 += kDqReduceRows)
+              tma_reduce_add_2d(&mapDQ, stage_base + qi * 4096 + h0 * 256, 0,
+                                tok[qi] * kQHeads + tv.g * kHeadsPerGroup + int(h0));
           bulk_commit();
           bulk_wait_read0();
           mbar_arrive(smem_u32(&bars.qdo_empty[st]));

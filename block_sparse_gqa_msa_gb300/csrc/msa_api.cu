@@ -164,13 +164,14 @@ CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T) {
 }
 
 // [rows, 128] 16-bit pool (dQ accumulation) as the destination of bulk
-// tensor reductions; box = 16 rows x 128 columns, no swizzle (dense 4 KB).
+// tensor reductions; box = kDqReduceRows rows x 128 columns, no swizzle
+// (dense rows of 256 bytes).
 CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows, bool bf16) {
   auto fn = encode_fn();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t gd[2] = {cuuint64_t(kHeadDim), cuuint64_t(rows)};
   cuuint64_t gs[1] = {cuuint64_t(kHeadDim * 2)};
-  cuuint32_t box[2] = {128, 16};
+  cuuint32_t box[2] = {128, kDqReduceRows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
             const_cast<void*>(base), gd, gs, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
