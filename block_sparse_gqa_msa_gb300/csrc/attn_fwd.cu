@@ -248,6 +248,78 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
 }
 
+// MMA issuer of k_fwd_main (one thread).  A function of its own so its few
+// live values stay in registers whatever the other roles need.
+__device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t sbase,
+                                          const int4* tasks, int64_t my_n, int chunk,
+                                          volatile int* abort_flag) {
+  constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T   (bf16)
+  constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, P in TMEM)
+  auto wait = [&](uint64_t& bar, uint32_t ph) {
+    return mbar_wait(smem_u32(&bar), ph, abort_flag);
+  };
+  // Descriptors are built once; a k-step only adds a constant to the
+  // start-address field (addresses stay below 256 KB, so the 14-bit field
+  // never carries).
+  const uint64_t kK = sdesc_sw128(sbase + kSmK, 16u, 1024u);     // K, K-major
+  const uint64_t mV = sdesc_sw128(sbase + kSmV, 16384u, 1024u);  // V (fp16), MN-major
+  const uint64_t kQ0 = sdesc_sw128(sbase + kSmQ, 16u, 1024u);
+  constexpr uint64_t kStage = kTileBytes >> 4;
+  auto kstep = [](int kk) { return uint64_t((kk >> 2) * 1024 + (kk & 3) * 2); };
+  auto mstep = [](int kk) { return uint64_t(kk) * 128u; };
+  int64_t kv_loads = 0;
+  bool ok = true, need_v = false;
+  // S(it) goes to stage it&1, whose P(it-2) must have been read by PV(it-2).
+  auto issue_S = [&](int64_t it) -> bool {
+    const int st = int(it & 1);
+    if (!wait(bars.q_full[st], uint32_t((it >> 1) & 1))) return false;
+    if (it >= 2 && !wait(bars.o_full[st], uint32_t(((it >> 1) - 1) & 1))) return false;
+    tc_fence_after();
+    const uint64_t bq = kQ0 + uint64_t(st) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(tmem + st * 128, bq + kstep(kk), kK + kstep(kk), idS, kk > 0);
+    umma_commit(smem_u32(&bars.s_full[st]));
+    umma_commit(smem_u32(&bars.q_empty[st]));
+    return true;
+  };
+  auto wait_kv = [&]() -> bool {
+    if (!wait(bars.kv_full, uint32_t(kv_loads & 1))) return false;
+    ++kv_loads;
+    need_v = true;
+    return true;
+  };
+  int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
+  int next_kv = task_rec(tasks, 1, my_n, chunk).w;
+  ok = wait_kv() && issue_S(0);
+  for (int64_t it = 0; ok && it < my_n; ++it) {
+    const int st = int(it & 1);
+    const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;
+    const bool same = (it + 1 < my_n) && next_kv == cur_kv;
+    if (same && !issue_S(it + 1)) break;
+    if (!wait(bars.p_full[st], uint32_t((it >> 1) & 1))) break;
+    if (it >= 2 && !wait(bars.o_free[st], uint32_t(((it >> 1) - 1) & 1))) break;
+    if (need_v) {
+      if (!wait(bars.v_ready, uint32_t((kv_loads - 1) & 1))) break;
+      need_v = false;
+    }
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ts(tmem + 256 + st * 128, tmem + st * 128 + kk * 8, mV + mstep(kk), idPV, kk > 0);
+    umma_commit(smem_u32(&bars.o_full[st]));
+    if (it + 1 < my_n && !same) {
+      umma_commit(smem_u32(&bars.kv_empty));
+      cur_kv = next_kv;
+      if (!wait_kv() || !issue_S(it + 1)) break;
+    }
+    next_kv = next2_kv;
+  }
+  // Make sure no MMA is still running before TMEM is released.
+  umma_commit(smem_u32(&bars.fin));
+  mbar_wait_drain(smem_u32(&bars.fin), 0);
+}
+
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_main(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV) {
@@ -357,76 +429,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T   (bf16)
-      constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, P in TMEM)
-      int64_t kv_loads = 0;
-      bool ok = true, need_v = false;
-      // S(it) goes to stage it&1, whose P(it-2) must have been read by PV(it-2).
-      auto issue_S = [&](int64_t it) -> bool {
-        const int st = int(it & 1);
-        if (!mbar_wait(smem_u32(&bars.q_full[st]), uint32_t((it >> 1) & 1), abort_flag))
-          return false;
-        if (it >= 2 &&
-            !mbar_wait(smem_u32(&bars.o_full[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t sq = sbase + kSmQ + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + st * 128, desc_kmajor(sq, kk), desc_kmajor(sbase + kSmK, kk), idS,
-                  kk > 0);
-        umma_commit(smem_u32(&bars.s_full[st]));
-        umma_commit(smem_u32(&bars.q_empty[st]));
-        return true;
-      };
-      auto wait_kv = [&]() -> bool {
-        if (!mbar_wait(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) return false;
-        ++kv_loads;
-        need_v = true;
-        return true;
-      };
-      int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
-      int next_kv = task_rec(tasks, 1, my_n, chunk).w;
-      ok = wait_kv() && issue_S(0);
-      for (int64_t it = 0; ok && it < my_n; ++it) {
-        const int st = int(it & 1);
-        const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;
-        const bool same = (it + 1 < my_n) && next_kv == cur_kv;
-        if (same && !issue_S(it + 1)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars.p_full[st]), uint32_t((it >> 1) & 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (it >= 2 &&
-            !mbar_wait(smem_u32(&bars.o_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (need_v) {
-          if (!mbar_wait(smem_u32(&bars.v_ready), uint32_t((kv_loads - 1) & 1), abort_flag)) {
-            ok = false;
-            break;
-          }
-          need_v = false;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + st * 128, tmem + st * 128 + kk * 8, desc_mnmajor(sbase + kSmV, kk),
-                  idPV, kk > 0);
-        umma_commit(smem_u32(&bars.o_full[st]));
-        if (it + 1 < my_n && !same) {
-          umma_commit(smem_u32(&bars.kv_empty));
-          cur_kv = next_kv;
-          if (!wait_kv() || !issue_S(it + 1)) { ok = false; break; }
-        }
-        next_kv = next2_kv;
-      }
-      // Make sure no MMA is still running before TMEM is released.
-      umma_commit(smem_u32(&bars.fin));
-      mbar_wait_drain(smem_u32(&bars.fin), 0);
-    }
+    if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, my_n, chunk, abort_flag);
   } else if (warp == 14) {
     // ---------------- V tile bf16 -> fp16 (scaled by an exact power of two)
     if (my_n > 0) {
@@ -788,7 +791,6 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   launch_begin("fwd_main", s);
   k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV);
   launch_end("fwd_main", s);
-  const int64_t rows = p.T * kQHeads;
   launch_begin("fwd_finalize", s);
   k_fwd_finalize<<<unsigned(device_sm_count() * 16), 256, 0, s>>>(
       p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o), lse, list);
