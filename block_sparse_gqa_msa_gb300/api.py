@@ -87,6 +87,8 @@ SIGNATURES = {
     "msa_profile_read": ([ctypes.c_char_p, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double)],
                          _I32),
     "msa_launch_count": ([], _I64),
+    "msa_pack_thd": ([_P, _I32, _I32, _I32, _P, _P, _P, _P], _I32),
+    "msa_unpack_bshd": ([_P, _I32, _I32, _I32, _P, _P, _P, _P], _I32),
 }
 
 
@@ -294,3 +296,49 @@ def profile_read(name: str):
 
 def launch_count() -> int:
     return int(lib().msa_launch_count())
+
+
+# ---------------------------------------------------------------- THD packing
+def _row_bytes(x: torch.Tensor, lead: int) -> int:
+    return int(x[(0,) * lead].numel() * x.element_size()) if x.numel() else 0
+
+
+def pack_thd(x: torch.Tensor, row_len: torch.Tensor, total: int | None = None, stream=None):
+    """Padded packed rows -> compact THD.
+
+    x: CUDA tensor [B, S, ...] (each token row a multiple of 16 bytes);
+    row_len: int32 [B] on the same device, tokens 0..row_len[b]-1 of row b are
+    real.  Returns (y [T, ...], row_offsets int32 [B+1]).  ``total`` = T if
+    known; otherwise it is read from row_len (one device-to-host copy).
+    """
+    if not (x.is_cuda and row_len.is_cuda):
+        raise ValueError("pack_thd needs CUDA tensors")
+    if x.dim() < 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [B, S, ...] tensor")
+    B, S = int(x.shape[0]), int(x.shape[1])
+    _need(row_len, "row_len", torch.int32, (B,))
+    if total is None:
+        total = int(row_len.clamp(0, S).sum().item())
+    y = torch.empty((total,) + tuple(x.shape[2:]), dtype=x.dtype, device=x.device)
+    offs = torch.empty(B + 1, dtype=torch.int32, device=x.device)
+    _check(lib().msa_pack_thd(_ptr(x), B, S, _row_bytes(x, 2), _ptr(row_len), _ptr(y),
+                              _ptr(offs), _stream(stream)), "msa_pack_thd")
+    return y, offs
+
+
+def unpack_bshd(y: torch.Tensor, row_len: torch.Tensor, row_offsets: torch.Tensor, S: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Compact THD -> padded packed rows [B, S, ...] (padding rows zero)."""
+    if not (y.is_cuda and row_len.is_cuda and row_offsets.is_cuda):
+        raise ValueError("unpack_bshd needs CUDA tensors")
+    if y.dim() < 1 or not y.is_contiguous():
+        raise ValueError("y must be a contiguous [T, ...] tensor")
+    B = int(row_len.shape[0])
+    _need(row_len, "row_len", torch.int32, (B,))
+    _need(row_offsets, "row_offsets", torch.int32, (B + 1,))
+    if out is None:
+        out = torch.empty((B, S) + tuple(y.shape[1:]), dtype=y.dtype, device=y.device)
+    row_bytes = int(out[0, 0].numel() * out.element_size())
+    _check(lib().msa_unpack_bshd(_ptr(y), B, S, row_bytes, _ptr(row_len), _ptr(row_offsets),
+                                 _ptr(out), _stream(stream)), "msa_unpack_bshd")
+    return out

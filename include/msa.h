@@ -221,6 +221,35 @@ msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* c
                            int64_t col_capacity, int32_t* tasks, int64_t task_capacity);
 
 /*
+ * Compaction of padded packed rows into the compact THD layout, and back
+ * (the steps either side of the operation when documents arrive packed into
+ * fixed-length rows with trailing padding: NeMo-Automodel PR "feat(minimax-m3):
+ * add SM100 MSA sparse attention with custom backward", section "Design" -
+ * padding tokens are dropped before the flat attention call and the output is
+ * scattered back).  The pages print no interface for them; these are plain
+ * row gathers.
+ *
+ *   x        [B][S][row_bytes] bytes, row b's tokens 0..row_len[b]-1 are real
+ *   row_len  int32 [B] device; each value must lie in [0, S] (values outside
+ *            are clamped into it)
+ *   y        [T][row_bytes] bytes, T = sum of row_len, rows in (b, s) order
+ *   row_offsets int32 [B+1] device: exclusive prefix sum of row_len
+ *            (written by msa_pack_thd, read by msa_unpack_bshd)
+ * row_bytes must be a positive multiple of 16 and all pointers 16-byte
+ * aligned; B >= 1, S >= 1, B * S < 2^31.  The caller sizes y for T rows (it
+ * knows the lengths; T <= B * S always suffices).  msa_unpack_bshd writes
+ * zeros into the padding rows of x.  Both are asynchronous on the stream.
+ * Errors: MSA_ERR_INVALID_ARG (null pointer, bad sizes), MSA_ERR_ALIGNMENT,
+ * MSA_ERR_CUDA (launch failure).
+ */
+msa_status msa_pack_thd(const void* x, int32_t B, int32_t S, int32_t row_bytes,
+                        const int32_t* row_len, void* y, int32_t* row_offsets,
+                        msa_stream_t stream);
+msa_status msa_unpack_bshd(const void* y, int32_t B, int32_t S, int32_t row_bytes,
+                           const int32_t* row_len, const int32_t* row_offsets, void* x,
+                           msa_stream_t stream);
+
+/*
  * Kernel timing for benchmarks.  While enabled, every kernel the library
  * launches is bracketed by CUDA events on its launch stream.  msa_profile_read
  * synchronises and returns, for the kernel family named (e.g. "fwd_main",

@@ -95,3 +95,12 @@ def test_python_binding_rejects_cpu_tensors():
     offs = torch.tensor([0, 10], dtype=torch.int32)
     with pytest.raises(ValueError):
         api.msa_build_plan(q2k, offs)
+
+
+def test_autograd_wrapper_needs_a_selection():
+    import torch
+    from block_sparse_gqa_msa_gb300.autograd import msa_attention
+    q = torch.zeros(4, 64, 128, dtype=torch.bfloat16)
+    k = torch.zeros(4, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        msa_attention(q, k, k)
