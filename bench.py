@@ -125,6 +125,46 @@ def recorded_traffic(kernel: str, workload: str):
     return rec.get("bytes_per_launch")
 
 
+# ---------------------------------------------------------------- adjacent steps
+def measure_packing(dev, peaks):
+    """Padded packed rows <-> compact THD for the query tensor of eight packed
+    rows of 16384 tokens (each row losing a U(0, 0.15) trailing fraction to
+    padding, as in the eight-row workload): device time per call with CUDA
+    events (inputs of 2 GB, far above L2), algorithmic bytes = the rows read
+    and written, against the measured copy bandwidth."""
+    from block_sparse_gqa_msa_gb300 import api
+    B, S = 8, 16384
+    rng = np.random.default_rng(4004)
+    lens = (S - np.floor(rng.uniform(0.0, 0.15, size=B) * S)).astype(np.int32)
+    row_len = torch.from_numpy(lens).to(dev)
+    x = torch.empty((B, S, 64, 128), dtype=torch.bfloat16, device=dev).normal_()
+    T = int(lens.sum())
+    row_bytes = 64 * 128 * 2
+    stream = torch.cuda.current_stream()
+    out = {}
+    y, offs = api.pack_thd(x, row_len, total=T)
+    back = api.unpack_bshd(y, row_len, offs, S)
+    for name, fn, nbytes in (
+            ("pack_thd", lambda: api.pack_thd(x, row_len, total=T), 2 * T * row_bytes),
+            ("unpack_bshd", lambda: api.unpack_bshd(y, row_len, offs, S, out=back),
+             (T + B * S) * row_bytes)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 10
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "bytes": nbytes, "GB_s": gbs,
+                     "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+                     "shape": f"[{B},{S},64,128] bf16, T={T}"}
+    del x, y, back
+    return out
+
+
 # ---------------------------------------------------------------- multi-rank
 def reduce_over_ranks(x: float, world: int, op: str = "max") -> float:
     """Max (the slowest rank's time) or sum (work done by all ranks) of one
@@ -374,6 +414,7 @@ def run_gpu(args, rank, world):
     peak = float(peaks["bf16_tflops"])
     traffic = recorded_traffic(dom, w.name)
 
+    adjacent = measure_packing(dev, peaks) if not args.no_adjacent else None
     cpu = cpu_sample(w, budget_s=20.0) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -399,6 +440,8 @@ def run_gpu(args, rank, world):
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"
                      if peak_src == "measured" else "fallback 1.9 PFLOP/s"},
     }
+    if adjacent:
+        line["adjacent"] = adjacent
     if cpu:
         line["cpu_baseline"] = {"value": cpu["flops"] / cpu["seconds"] / 1e12, "unit": "TFLOP/s",
                                 "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]}
@@ -414,6 +457,8 @@ def main():
     ap.add_argument("--super-block", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-adjacent", action="store_true",
+                    help="skip the THD packing measurement")
     ap.add_argument("--sample-seconds", type=float, default=0.0,
                     help="reference arm: CPU seconds per step (default: about 30 s per run)")
     ap.add_argument("--sample-max-tokens", type=int, default=0,
