@@ -162,7 +162,52 @@ def measure_packing(dev, peaks):
                      "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
                      "shape": f"[{B},{S},64,128] bf16, T={T}"}
     del x, y, back
+    out["select_blocks"] = measure_selection(dev, peaks)
     return out
+
+
+def measure_selection(dev, peaks, dim: int = 64):
+    """Block scorer + top-16 on the packed-document T=16384 row with index
+    dim 64 (synthetic N(0,1) index queries / keys): device time per call and
+    the scoring FMA rate against the fp32 FMA peak (152 SMs x 128 lanes x the
+    maximum SM clock)."""
+    from block_sparse_gqa_msa_gb300 import api
+    w = inputs.config(WORKLOAD)
+    T = w.T
+    g = torch.Generator().manual_seed(7007)
+    iq = torch.randn(T, 4, dim, generator=g).to(torch.bfloat16).to(dev)
+    ik = torch.randn(T, 4, dim, generator=g).to(torch.bfloat16).to(dev)
+    offs = w.doc_offsets.to(dev)
+    q2k = torch.empty((4, T, 16), dtype=torch.int32, device=dev)
+    ws = torch.empty(api.select_workspace_bytes(T, w.num_docs, dim), dtype=torch.uint8,
+                     device=dev)
+    # scoring work: every (token, index head) with more than 16 candidate blocks
+    # scores blocks 1 .. b-1 (blocks 0 and b are always kept)
+    fma = 0
+    for ln in np.diff(w.doc_offsets.numpy()):
+        b = np.arange(int(ln)) // 128
+        fma += int(np.where(b + 1 > 16, b - 1, 0).sum()) * 4 * dim
+    fma += T * 4 * dim  # block sums
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        api.msa_select_blocks(iq, ik, offs, q2k=q2k, workspace=ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        api.msa_select_blocks(iq, ik, offs, q2k=q2k, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 10
+    api.profile_enable(True)
+    api.profile_reset()
+    api.msa_select_blocks(iq, ik, offs, q2k=q2k, workspace=ws)
+    split = {k: api.profile_read(k)[1] for k in ("sel_summary", "sel_topk")}
+    api.profile_enable(False)
+    peak = 152 * 128 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    return {"ms": ms, "fma": fma, "TFMA_s": fma / (ms * 1e-3) / 1e12,
+            "frac_of_fp32_fma": fma / (ms * 1e-3) / peak, "bound": "alu",
+            "kernels_ms": {k: round(v, 4) for k, v in split.items()},
+            "shape": f"T={T}, {w.num_docs} documents, index dim {dim}"}
 
 
 # ---------------------------------------------------------------- multi-rank

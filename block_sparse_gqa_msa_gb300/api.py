@@ -89,6 +89,8 @@ SIGNATURES = {
     "msa_launch_count": ([], _I64),
     "msa_pack_thd": ([_P, _I32, _I32, _I32, _P, _P, _P, _P], _I32),
     "msa_unpack_bshd": ([_P, _I32, _I32, _I32, _P, _P, _P, _P], _I32),
+    "msa_select_workspace_bytes": ([_I64, _I32, _I32, ctypes.POINTER(_SZ)], _I32),
+    "msa_select_blocks": ([_P, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _SZ, _P], _I32),
 }
 
 
@@ -342,3 +344,35 @@ def unpack_bshd(y: torch.Tensor, row_len: torch.Tensor, row_offsets: torch.Tenso
     _check(lib().msa_unpack_bshd(_ptr(y), B, S, row_bytes, _ptr(row_len), _ptr(row_offsets),
                                  _ptr(out), _stream(stream)), "msa_unpack_bshd")
     return out
+
+
+# ---------------------------------------------------------------- block selection
+def select_workspace_bytes(T: int, num_docs: int, dim: int) -> int:
+    n = _SZ(0)
+    _check(lib().msa_select_workspace_bytes(T, num_docs, dim, ctypes.byref(n)),
+           "msa_select_workspace_bytes")
+    return int(n.value)
+
+
+def msa_select_blocks(iq: torch.Tensor, ik: torch.Tensor, doc_offsets: torch.Tensor,
+                      force_local: bool = True, q2k: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q2k int32 [4, T, 16] from index queries / keys bf16 [T, 4, dim] (see
+    msa_select_blocks in include/msa.h for the scoring and tie rules)."""
+    if iq.dim() != 3:
+        raise ValueError("iq must be [T, 4, dim]")
+    T, dim = int(iq.shape[0]), int(iq.shape[2])
+    _need(iq, "iq", torch.bfloat16, (T, NUM_KV_HEADS, dim))
+    _need(ik, "ik", torch.bfloat16, (T, NUM_KV_HEADS, dim))
+    D = int(doc_offsets.numel()) - 1
+    _need(doc_offsets, "doc_offsets", torch.int32, (D + 1,))
+    if q2k is None:
+        q2k = torch.empty((NUM_KV_HEADS, T, TOPK), dtype=torch.int32, device=iq.device)
+    _need(q2k, "q2k", torch.int32, (NUM_KV_HEADS, T, TOPK))
+    if workspace is None:
+        workspace = torch.empty(select_workspace_bytes(T, D, dim), dtype=torch.uint8,
+                                device=iq.device)
+    _check(lib().msa_select_blocks(_ptr(iq), _ptr(ik), T, dim, _ptr(doc_offsets), D,
+                                   1 if force_local else 0, _ptr(q2k), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "msa_select_blocks")
+    return q2k

@@ -250,6 +250,36 @@ msa_status msa_unpack_bshd(const void* y, int32_t B, int32_t S, int32_t row_byte
                            msa_stream_t stream);
 
 /*
+ * Block selection: the index scorer and top-16 choice that produce q2k (the
+ * step upstream of the plan: NeMo-Automodel PR "feat(minimax-m3): add SM100
+ * MSA sparse attention with custom backward", sections "Summary" and
+ * "Design" - an indexer picks, per query and index head, the top-16
+ * document-local key blocks).  The pages give no scoring formula; this call
+ * implements the plainest reading:
+ *   summary(g, d, v) = mean of the index keys ik[j, g, :] of document block v
+ *   score(t, g, v)   = dot(iq[t, g, :], summary(g, d, v))  for v = 0 .. b,
+ * b = the query's own block.  With b + 1 <= 16 all candidates are selected;
+ * otherwise the 16 best by (score descending, block ascending), and with
+ * force_local != 0 blocks 0 and b are always kept (plus the 14 best of
+ * 1 .. b-1).  Slots hold the blocks in ascending order, then -1.  Scores are
+ * fp32: block sums key by key divided by the key count, dot products channel
+ * by channel with fused multiply-adds (a fixed order, so the ranking is
+ * reproducible).
+ *   iq, ik       bf16 [T][4][dim] device, dim in {8, 16, ..., 128}; finite
+ *   doc_offsets  int32 [num_docs+1] device, valid as for msa_build_plan
+ *   q2k          int32 [4][T][16] device (output)
+ *   workspace    msa_select_workspace_bytes(T, num_docs, dim) bytes, 16-byte
+ *                aligned (block summaries)
+ * Asynchronous on the stream.  Errors: MSA_ERR_INVALID_ARG, MSA_ERR_ALIGNMENT,
+ * MSA_ERR_WORKSPACE, MSA_ERR_CUDA.
+ */
+msa_status msa_select_workspace_bytes(int64_t T, int32_t num_docs, int32_t dim, size_t* bytes);
+msa_status msa_select_blocks(const void* iq, const void* ik, int64_t T, int32_t dim,
+                             const int32_t* doc_offsets, int32_t num_docs, int32_t force_local,
+                             int32_t* q2k, void* workspace, size_t workspace_bytes,
+                             msa_stream_t stream);
+
+/*
  * Kernel timing for benchmarks.  While enabled, every kernel the library
  * launches is bracketed by CUDA events on its launch stream.  msa_profile_read
  * synchronises and returns, for the kernel family named (e.g. "fwd_main",

@@ -87,6 +87,8 @@ def _bind(lib):
     lib.oracle_plan.argtypes = [_P, _I64, _P, _I32, _I32, _P, _P, _P, _I64, _P, _I64, _P, _I64, _P]
     lib.oracle_pair_count.argtypes = [_P, _I64, _P, _I32]
     lib.oracle_pair_count.restype = _I64
+    lib.oracle_select_blocks.argtypes = [_P, _P, _I64, _I32, _P, _I32, _I32, _P]
+    lib.oracle_select_blocks.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     for f in ("oracle_forward", "oracle_dq", "oracle_dkv_blocks", "oracle_backward",
@@ -254,3 +256,19 @@ def pair_count(q2k, doc_offsets, T: int) -> int:
 def threads() -> int:
     """OpenMP threads the oracle uses."""
     return int(_load().oracle_threads())
+
+
+def select_blocks(iq, ik, doc_offsets, force_local: bool = True) -> np.ndarray:
+    """q2k int32 [4, T, 16] chosen by the block scorer (see oracle_select_blocks
+    in msa_oracle.c).  iq, ik: bf16 [T, 4, dim] tensors or uint16 bit arrays."""
+    a = _bf16_bits(iq)
+    b = _bf16_bits(ik)
+    if a.shape != b.shape or a.ndim != 3 or a.shape[1] != 4:
+        raise ValueError("iq and ik must both be [T, 4, dim]")
+    T, _, dim = a.shape
+    offs = _i32(doc_offsets)
+    q2k = np.zeros((4, T, 16), dtype=np.int32)
+    rc = _load().oracle_select_blocks(_ptr(a), _ptr(b), T, dim, _ptr(offs), offs.size - 1,
+                                      1 if force_local else 0, _ptr(q2k))
+    _check(rc, "select_blocks")
+    return q2k

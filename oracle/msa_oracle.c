@@ -516,3 +516,114 @@ int oracle_threads(void) {
   return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * Block selection: the index scorer and top-k that produce q2k.
+ *
+ * The pages name the step (an indexer scores the key blocks, each query
+ * keeps the top 16) but print no scoring formula; the plainest reading, used
+ * here and in the kernel:
+ *   summary(g, d, v)[c] = mean over the keys j of document block v of
+ *                         ik[j, g, c]   (block v = document positions
+ *                         128v .. 128v+127, the last one may be partial)
+ *   score(t, g, v)      = sum_c iq[t, g, c] * summary(g, d, v)[c]
+ * over the candidate blocks v = 0 .. b of the query's document (b = its own
+ * block).  With b + 1 <= 16 every candidate is selected.  Otherwise the 16
+ * best by (score descending, block ascending) are kept; with force_local the
+ * sink block 0 and the query's own block b are always kept and 14 are chosen
+ * among 1 .. b-1.  Slots hold the chosen blocks in ascending order, then -1.
+ *
+ * A ranking is decided by floating point, so this takes the decisions in the
+ * kernel's precision and order of operations: fp32, the block sum
+ * accumulated key by key (acc += x) and divided by the key count, the score
+ * accumulated channel by channel with fused multiply-adds.
+ * iq, ik: bf16 bit patterns [T][4][dim]; q2k: [4][T][16].
+ */
+static float bf16_to_f32(uint16_t u) {
+  uint32_t w = (uint32_t)u << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return f;
+}
+
+/* (s1, v1) ranks before (s2, v2)? */
+static int sel_better(float s1, int32_t v1, float s2, int32_t v2) {
+  return s1 > s2 || (s1 == s2 && v1 < v2);
+}
+
+int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int32_t dim,
+                         const int32_t* offs, int32_t D, int32_t force_local, int32_t* q2k) {
+  if (T <= 0 || dim <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  int64_t maxnb = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (nblocks(offs[d + 1] - offs[d]) > maxnb) maxnb = nblocks(offs[d + 1] - offs[d]);
+  int err = 0;
+#pragma omp parallel
+  {
+    float* summ = (float*)malloc(sizeof(float) * (size_t)maxnb * (size_t)dim);
+    float* score = (float*)malloc(sizeof(float) * (size_t)maxnb);
+    int32_t cached_doc = -1, cached_g = -1;
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t i = 0; i < 4 * T; ++i) {
+      const int g = (int)(i / T);
+      const int64_t t = i % T;
+      const int32_t d = doc_of(offs, D, t);
+      const int64_t s0 = offs[d];
+      const int32_t len = offs[d + 1] - offs[d];
+      const int32_t nb = nblocks(len);
+      const int32_t b = (int32_t)((t - s0) / BLK);
+      int32_t* out = q2k + ((int64_t)g * T + t) * TOPK;
+      if (b + 1 <= TOPK) {
+        for (int k = 0; k < TOPK; ++k) out[k] = k <= b ? k : -1;
+        continue;
+      }
+      if (d != cached_doc || g != cached_g) { /* block summaries of (g, d) */
+        for (int32_t v = 0; v < nb; ++v) {
+          const int32_t n = (len - v * BLK) < BLK ? (len - v * BLK) : BLK;
+          for (int32_t c = 0; c < dim; ++c) {
+            float acc = 0.f;
+            for (int32_t j = 0; j < n; ++j)
+              acc += bf16_to_f32(ik[((s0 + (int64_t)v * BLK + j) * NKV + g) * dim + c]);
+            summ[(int64_t)v * dim + c] = acc / (float)n;
+          }
+        }
+        cached_doc = d;
+        cached_g = g;
+      }
+      for (int32_t v = 0; v <= b; ++v) {
+        float acc = 0.f;
+        for (int32_t c = 0; c < dim; ++c)
+          acc = fmaf(bf16_to_f32(iq[(t * NKV + g) * dim + c]), summ[(int64_t)v * dim + c], acc);
+        score[v] = acc;
+      }
+      /* selection by repeated best-of-the-rest */
+      unsigned char* taken = (unsigned char*)calloc((size_t)b + 1, 1);
+      int32_t chosen[TOPK];
+      int nc = 0;
+      if (force_local) {
+        chosen[nc++] = 0;
+        chosen[nc++] = b;
+        taken[0] = taken[b] = 1;
+      }
+      while (nc < TOPK) {
+        int32_t best = -1;
+        for (int32_t v = 0; v <= b; ++v)
+          if (!taken[v] && (best < 0 || sel_better(score[v], v, score[best], best))) best = v;
+        if (best < 0) break;
+        taken[best] = 1;
+        chosen[nc++] = best;
+      }
+      free(taken);
+      for (int x = 1; x < nc; ++x) /* ascending */
+        for (int y = x; y > 0 && chosen[y - 1] > chosen[y]; --y) {
+          int32_t tmp = chosen[y];
+          chosen[y] = chosen[y - 1];
+          chosen[y - 1] = tmp;
+        }
+      for (int k = 0; k < TOPK; ++k) out[k] = k < nc ? chosen[k] : -1;
+    }
+    free(summ);
+    free(score);
+  }
+  return err;
+}

@@ -104,3 +104,15 @@ def test_autograd_wrapper_needs_a_selection():
     k = torch.zeros(4, 4, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         msa_attention(q, k, k)
+
+
+def test_select_workspace_host_checks(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.msa_select_workspace_bytes(16384, 7, 64, ctypes.byref(n)) == 0
+    assert n.value == 4 * (16384 // 128 + 7 + 1) * 64 * 4
+    for T, D, dim in ((0, 1, 64), (100, 0, 64), (100, 1, 12), (100, 1, 136), (100, 1, 0)):
+        assert lib.msa_select_workspace_bytes(T, D, dim, ctypes.byref(n)) == 1
+    g = ctypes.c_void_p(0x10000)
+    assert lib.msa_select_blocks(g, g, 100, 64, g, 1, 1, g, g, 16, None) == 4   # workspace
+    assert lib.msa_select_blocks(ctypes.c_void_p(0x10008), g, 100, 64, g, 1, 1, g, g, 1 << 20,
+                                 None) == 3                                     # alignment

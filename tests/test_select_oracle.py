@@ -1,0 +1,89 @@
+"""Pins for the block-selection oracle (index scorer + top-k):
+
+  * a closed form: every key of block v equals val_v * e_0 and iq = e_0, so a
+    block's score is exactly val_v and the selection is the best val_v;
+  * ties go to the lower block index;
+  * queries whose document has at most 16 candidate blocks take them all;
+  * on random inputs, the chosen blocks' scores (recomputed here in fp64 from
+    the bf16 values) all rank at or above every unchosen block, up to fp32
+    rounding, and the output is sorted, distinct and causal.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+DIM = 8
+
+
+def _closed_form_inputs(block_vals_per_doc):
+    """ik rows of block v of doc d all equal val * e_0; iq = e_0."""
+    lens = [128 * len(vals) for vals in block_vals_per_doc]
+    T = sum(lens)
+    ik = torch.zeros(T, 4, DIM)
+    t = 0
+    for vals in block_vals_per_doc:
+        for val in vals:
+            ik[t:t + 128, :, 0] = float(val)
+            t += 128
+    iq = torch.zeros(T, 4, DIM)
+    iq[:, :, 0] = 1.0
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return iq.to(torch.bfloat16), ik.to(torch.bfloat16), offs
+
+
+@pytest.mark.parametrize("force_local", [True, False])
+def test_closed_form_selection(oracle_mod, force_local):
+    rng = np.random.default_rng(3)
+    docs = [(rng.permutation(40) - 20) / 4.0, (rng.permutation(24) - 12) / 4.0]
+    iq, ik, offs = _closed_form_inputs(docs)
+    q2k = oracle_mod.select_blocks(iq, ik, offs, force_local=force_local)
+    for d, vals in enumerate(docs):
+        for b in range(len(vals)):
+            t = int(offs[d]) + 128 * b + 77
+            if b + 1 <= 16:
+                expect = list(range(b + 1))
+            else:
+                pool = list(range(1, b)) if force_local else list(range(b + 1))
+                pool.sort(key=lambda v: (-vals[v], v))
+                keep = pool[:14] if force_local else pool[:16]
+                expect = sorted(keep + ([0, b] if force_local else []))
+            for g in range(4):
+                got = [x for x in q2k[g, t] if x != -1]
+                assert got == expect, (d, b, g)
+
+
+def test_ties_prefer_lower_blocks(oracle_mod):
+    iq, ik, offs = _closed_form_inputs([[1.0] * 30])
+    q = oracle_mod.select_blocks(iq, ik, offs, force_local=False)
+    assert q[0, 128 * 29].tolist() == list(range(16))
+    q = oracle_mod.select_blocks(iq, ik, offs, force_local=True)
+    assert q[1, 128 * 29 + 5].tolist() == list(range(15)) + [29]
+
+
+def test_random_selection_is_a_valid_top_k(oracle_mod):
+    g = torch.Generator().manual_seed(11)
+    lens = [2500, 300, 4100]
+    T = sum(lens)
+    iq = torch.randn(T, 4, DIM, generator=g).to(torch.bfloat16)
+    ik = torch.randn(T, 4, DIM, generator=g).to(torch.bfloat16)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q2k = oracle_mod.select_blocks(iq, ik, offs, force_local=False)
+    qf, kf = iq.double().numpy(), ik.double().numpy()
+    rng = np.random.default_rng(0)
+    for t in rng.integers(0, T, size=60):
+        d = int(np.searchsorted(offs, t, side="right") - 1)
+        s0, n = int(offs[d]), int(lens[d])
+        b = (t - s0) // 128
+        for gg in range(4):
+            sel = [int(x) for x in q2k[gg, t] if x != -1]
+            assert sel == sorted(set(sel)) and all(0 <= v <= b for v in sel)
+            assert len(sel) == min(16, b + 1)
+            if b + 1 <= 16:
+                continue
+            summ = np.stack([kf[s0 + 128 * v:s0 + min(n, 128 * v + 128), gg].mean(0)
+                             for v in range(b + 1)])
+            sc = summ @ qf[t, gg]
+            unsel = [v for v in range(b + 1) if v not in sel]
+            assert sc[sel].min() >= sc[unsel].max() - 1e-4 * (1 + np.abs(sc).max())
