@@ -165,7 +165,7 @@ def plan_workspace_bytes(T: int, num_docs: int) -> int:
     return int(n.value)
 
 
-def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 16,
+def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 64,
                    workspace: torch.Tensor | None = None, stream=None,
                    dq_accum: str = "f16") -> Plan:
     """Device-side plan from q2k int32 [4,T,16] and doc_offsets int32 [D+1].
@@ -187,7 +187,7 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
     return Plan(st, workspace, q2k, doc_offsets)
 
 
-def msa_build_plan_static(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 16,
+def msa_build_plan_static(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 64,
                           stream=None, dq_accum: str = "f16") -> Plan:
     """Like msa_build_plan, but the plan tables live in the library's own
     static device array, so nothing is allocated.  For callers that cannot

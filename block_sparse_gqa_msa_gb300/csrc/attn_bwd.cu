@@ -716,7 +716,7 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
     }
     attr_set = true;
   }
-  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 16,
+  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 64,
                 p.dq_accum};
   launch_begin("bwd_main", s);
   const unsigned grid = unsigned(device_sm_count());

@@ -787,7 +787,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  FwdParams prm{p, M2, vmax, pool, lsum, c2, 8};
+  FwdParams prm{p, M2, vmax, pool, lsum, c2, 16};
   launch_begin("fwd_main", s);
   k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV);
   launch_end("fwd_main", s);

@@ -213,7 +213,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
                           size_t workspace_bytes, msa_stream_t stream, msa_plan* out) {
   if (!q2k || !doc_offsets || !workspace || !out) return MSA_ERR_INVALID_ARG;
   if (T < 1 || T > kMaxTokens || num_docs < 1 || num_docs > T) return MSA_ERR_INVALID_ARG;
-  const int32_t Z = opts ? opts->super_block : 16;
+  const int32_t Z = opts ? opts->super_block : 64;
   const int32_t acc = opts ? opts->dq_accum : MSA_DQ_ACCUM_F16;
   if (Z < 0 || acc < MSA_DQ_ACCUM_F16 || acc > MSA_DQ_ACCUM_F32) return MSA_ERR_INVALID_ARG;
   if (!aligned16(q2k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(doc_offsets) & 3u))

@@ -1,9 +1,10 @@
 // plan.cu - device-side plan builder: q2k -> k2q CSR -> task table.
 //
-// The pages describe this step as the official CSR builder plus the fused
-// task builder that "keeps exact counts and CTA scheduling on the device"
+// The pages describe this step as the official CSR builder plus a fused
+// task builder whose exact counts and CTA schedule never leave the device
 // (NeMo-Automodel PR "feat(minimax-m3) ...", Changelog; API page
-// msa_backward_sm100: task rows of 8 queries x 16 main heads bucketed by
+// msa_backward_sm100: tiles of 8 queries times the 16 query heads of an index
+// head, grouped by
 // (batch, index_head, key_block)).  Everything here stays on the device and
 // is launched with capacity-bounded grids; exact counts are read from the
 // plan header.

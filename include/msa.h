@@ -70,8 +70,8 @@ typedef enum msa_status {
 const char* msa_status_string(msa_status s);
 
 /* Precision of the dQ accumulation pool of msa_backward.  The pages' default
- * is packed FP16 atomics with a BF16 switch for range ("Supported scope":
- * MSA_M3_DQ_ACCUM); FP32 is the widest and slowest. */
+ * is packed FP16 atomics with a BF16 switch for range (section "Supported
+ * scope", the MSA_M3_DQ_ACCUM setting); FP32 is the widest and slowest. */
 typedef enum msa_dq_accum {
   MSA_DQ_ACCUM_F16 = 0,
   MSA_DQ_ACCUM_BF16 = 1,
@@ -81,7 +81,7 @@ typedef enum msa_dq_accum {
 /* Plan-build options.  Pass NULL for the defaults. */
 typedef struct msa_plan_options {
   /* Tasks of one (index head, key block) bucket are cut at runs of
-   * super_block consecutive query blocks (0 = never cut).  Default 16. */
+   * super_block consecutive query blocks (0 = never cut).  Default 64. */
   int32_t super_block;
   /* An msa_dq_accum value.  Default MSA_DQ_ACCUM_F16. */
   int32_t dq_accum;
@@ -93,9 +93,9 @@ typedef struct msa_plan_options {
  * head and key block, the queries that selected it (the k2q CSR), and the
  * task table of 128-row tiles (8 queries x 16 heads of one index head against
  * one key block) that the forward and backward kernels walk.  The pages call
- * these the CSR / scheduler metadata and the backward task rows
- * (msa_backward_sm100: "task rows (8 queries x 16 main heads = one 128-row
- * tile) bucketed by (batch, index_head, key_block)").
+ * these the CSR and scheduling metadata and, on the API page
+ * msa_backward_sm100, the backward's task rows, one 128-row tile each,
+ * grouped by (batch, index head, key block).
  *
  * A plain struct of device pointers into the caller's plan workspace and of
  * host-side capacities.  Fill it with msa_build_plan; do not edit it.  It
@@ -173,7 +173,7 @@ msa_status msa_build_plan_static(const int32_t* q2k, const int32_t* doc_offsets,
 msa_status msa_forward_workspace_bytes(const msa_plan* plan, size_t* bytes);
 
 /*
- * Forward (the pages' "flat sparse forward": O [T,64,128] and LSE [T,64]).
+ * Forward (the pages' flat sparse forward: O [T,64,128] and LSE [T,64]).
  *   q  device bf16 [T,64,128]; k, v device bf16 [T,4,128]
  *   softmax_scale   e.g. 1/sqrt(128)
  *   o   device bf16 [T,64,128] (written)

@@ -13,9 +13,9 @@
  *         Q[T,64,128], K/V[T,4,128], int32 q2k[4,T,16], -1 for unused slots,
  *         layout = document offsets) and "Supported scope" (64 query / 4 KV /
  *         4 index heads, head dim 128, block 128, top-k 16, causal prefill).
- *   [BWD] API page "msa_backward_sm100" - module description (task rows of
- *         8 queries x 16 main heads bucketed by (index_head, key_block);
- *         delta preprocess), run_backward parameter list (LSE is FP32 [T,64]).
+ *   [BWD] API page "msa_backward_sm100" - module description (tiles of 8
+ *         queries times the 16 query heads of an index head, grouped by index
+ *         head and key block; the delta preprocess), run_backward parameter list (LSE is FP32 [T,64]).
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - query head h uses KV head and index head h/16;

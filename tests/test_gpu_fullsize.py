@@ -1,6 +1,6 @@
 """Parity at the full sizes of the four large workloads (single 16k document,
 packed 16k row, eight packed rows of 16k, one 128k document), in the launch
-configuration the benchmark times (super-block 16, fp16 dQ pool, persistent
+configuration the benchmark times (super-block 64, fp16 dQ pool, persistent
 grids): the whole problem runs on the GPU, and sampled outputs are compared
 with the fp64 oracle computed one by one on the same inputs —
 
@@ -75,7 +75,7 @@ def sample_blocks(q2k: np.ndarray, offs: np.ndarray, rng: np.random.Generator, w
 
 def run_like_bench(w):
     q, k, v, do = (x.to(DEV) for x in (w.q, w.k, w.v, w.do))
-    plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=16)
+    plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=64)
     o, lse = api.msa_forward(plan, q, k, v, w.scale)
     dq, dk, dv = api.msa_backward(plan, q, k, v, o, lse, do, w.scale)
     torch.cuda.synchronize()
