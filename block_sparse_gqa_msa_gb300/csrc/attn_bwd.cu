@@ -10,23 +10,27 @@
 //   dV  += P^T dO,  dK += dS^T Q   (A operands read from TMEM; cols 256, 384)
 //   dQ^T = K^T dS^T                 (dS from shared memory; cols [128,256))
 // TMEM lane = key for S/dP/dV/dK, so the per-key softmax work is one thread
-// per key; lane = head dimension for dQ^T, so one warp reduces 32 consecutive
-// dQ elements of a row at a time (coalesced).  dV / dK accumulate over a run
-// of tasks that share the K/V block and are flushed with fp32 L2 reductions;
-// dQ is reduced per tile into an fp16 (default), bf16 or fp32 pool.
+// per key; lane = head dimension for dQ^T, so a warp adds 32 consecutive head
+// dimensions of a pair of query heads at a time.  dV / dK accumulate over a
+// run of tasks that share the K/V block and are flushed with fp32 L2
+// reductions.  dQ goes straight from registers into a head-pair-interleaved
+// pool (the two heads of a pair side by side per head dimension) with packed
+// 16-bit atomics (fp16 by default, bf16 or fp32 on request): each warp-wide
+// atomic covers 128 contiguous bytes, and no shared memory is involved.
 //
 // bwd_main runs 14 warps: a TMA producer, an MMA issuer, eight compute warps
-// (P^T, dS^T; two per TMEM lane quadrant, each owning 64 q-rows) and four
-// reduce warps (dQ^T staging + bulk tensor reduction, dV / dK flush).
+// (P^T, dS^T, dQ^T readout; two per TMEM lane quadrant, each owning 64
+// q-rows) and four warps that flush dV / dK at the end of each run.
 //
 // Kernels, in launch order:
 //   bwd_delta     delta = rowsum(dO * O); zero the dQ / dK / dV pools
 //   bwd_main      the tensor-core tile loop
-//   bwd_finalize  pools -> bf16 dQ, dK, dV
+//   bwd_finalize  pools -> bf16 dQ (de-interleaved), dK, dV
 #include "common.cuh"
 #include "sm100.cuh"
 
 #include <cstring>
+#include <type_traits>
 
 namespace msa {
 namespace {
@@ -108,17 +112,21 @@ constexpr uint32_t kTileBytes = 32768;
 constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmDO = 131072, kSmDS = 196608;
 constexpr uint32_t kBwdSmem = kSmDS + kTileBytes + 1024;
 
-// TMEM columns.  P^T of q-rows [64h, 64h+64) is packed into S^T columns
-// [64h, 64h+32) and dS^T into dP^T columns [128+64h, 128+64h+32), so each
-// compute half only overwrites S^T / dP^T columns it has already read.
+// TMEM columns.  S^T goes to [0,128).  For the q-rows [64h, 64h+64) of
+// compute half h, P^T is packed (bf16 pairs) into S^T columns [64h, 64h+32)
+// and dS^T into [64h+32, 64h+64): each half only overwrites S^T columns it
+// has already read.  dP^T goes to [128,256) and, once the compute warps have
+// read it, dQ^T of the same task.  dV and dK accumulate in [256,384) and
+// [384,512) over a run of tasks on one key block.
 constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDV = 256, kTmDK = 384;
-constexpr uint32_t kTmP = 0, kTmDST = 128, kTmDQ = 128;
-// A-operand column of k-step kk (q-rows 16kk..16kk+15) for P^T / dS^T.
+constexpr uint32_t kTmP = 0, kTmDS = 32, kTmDQ = 128;
+// A-operand column of k-step kk (q-rows 16kk..16kk+15) for P^T (add kTmDS
+// for dS^T).
 __device__ __forceinline__ uint32_t ts_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full, pds_full[2], dk_done, dv_done,
-      dq_full, dq_free, dkv_free, fin;
+  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], s_full, dp_full, p_ready[2],
+      ds_ready[2], pt_free, dq_full, dq_free, seg_done, dkv_free, cols, fin;
 };
 
 struct BwdParams {
@@ -156,15 +164,20 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
 // MMA issuer of k_bwd_main (one thread).  A function of its own so its few
 // live values stay in registers whatever the compute roles need.
 //
-// Per task t (waits in brackets):
-//   [dq_free(t-1)] dP^T(t)  [pds_0] dK, dV k-steps of q-rows 0-63
-//   [pds_1] dK, dV k-steps of q-rows 64-127  [dk_done] dQ^T(t)  [dv_done] S^T(t+1)
-// so the GEMMs of the first half overlap the softmax of the second.
+// Issue order for task t (waits in brackets):
+//   S^T(t), dP^T(t)                          (issued at the end of task t-1)
+//   [p_ready 0] dV k-steps of q-rows 0-63   [p_ready 1] q-rows 64-127
+//   [ds_ready 0] dK k-steps of q-rows 0-63  [ds_ready 1] q-rows 64-127
+//   dQ^T(t) into the dP^T columns (the compute warps have read dP^T(t))
+//   [pt_free] S^T(t+1)  [dq_free] dP^T(t+1)
+// The compute warps exponentiate S^T(t) while dP^T(t) runs, dV(t) starts as
+// soon as P^T(t) is in TMEM, and the compute warps read dQ^T(t) out while
+// S^T(t+1) runs.
 __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t sbase,
                                           const int4* tasks, int64_t my_n, int chunk,
                                           volatile int* abort_flag) {
   constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
-  constexpr uint32_t idTS = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
+  constexpr uint32_t idKM = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
   constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T
   auto wait = [&](uint64_t& bar, uint32_t ph) {
     const bool ok = mbar_wait(smem_u32(&bar), ph, abort_flag);
@@ -192,25 +205,29 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ss(tmem + kTmS, kK + kstep(kk), b + kstep(kk), idKK, kk > 0);
+    umma_commit(smem_u32(&bars.s_full));
   };
   auto issue_dP = [&](int64_t t) {
     const uint64_t b = kDO0 + uint64_t(t & 1) * kStage;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ss(tmem + kTmDP, kV + kstep(kk), b + kstep(kk), idKK, kk > 0);
-    umma_commit(smem_u32(&bars.sdp_full));
+    umma_commit(smem_u32(&bars.dp_full));
   };
-  // dK += dS^T Q and dV += P^T dO over the four k-steps of one half of the q-rows
-  auto issue_dkdv = [&](int64_t t, int h, uint32_t acc0) {
-    const uint64_t bq = mQ0 + uint64_t(t & 1) * kStage;
+  // dV += P^T dO over the four k-steps of one half of the q-rows
+  auto issue_dv = [&](int64_t t, int h, uint32_t acc0) {
     const uint64_t bo = mDO0 + uint64_t(t & 1) * kStage;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      umma_ts(tmem + kTmDK, tmem + kTmDST + ts_col(4 * h + j), bq + mstep(4 * h + j), idTS,
+      umma_ts(tmem + kTmDV, tmem + kTmP + ts_col(4 * h + j), bo + mstep(4 * h + j), idKM,
               j > 0 ? 1u : acc0);
+  };
+  // dK += dS^T Q over the four k-steps of one half of the q-rows
+  auto issue_dk = [&](int64_t t, int h, uint32_t acc0) {
+    const uint64_t bq = mQ0 + uint64_t(t & 1) * kStage;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      umma_ts(tmem + kTmDV, tmem + kTmP + ts_col(4 * h + j), bo + mstep(4 * h + j), idTS,
+      umma_ts(tmem + kTmDK, tmem + kTmP + kTmDS + ts_col(4 * h + j), bq + mstep(4 * h + j), idKM,
               j > 0 ? 1u : acc0);
   };
   int64_t kv_loads = 1, seg_done = 0;
@@ -218,30 +235,37 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
   int next_kv = task_rec(tasks, 1, my_n, chunk).w;
   bool ok = wait(bars.kv_full, 0) && wait(bars.qdo_full[0], 0);
-  if (ok) issue_S(0);
+  if (ok) {
+    issue_S(0);
+    issue_dP(0);
+  }
   for (int64_t it = 0; ok && it < my_n; ++it) {
     const uint32_t ph = uint32_t(it & 1);
     const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;  // used next iteration
-    // dP^T(it) overwrites dQ^T(it-1): the reducers must have read it.
-    if (it >= 1 && !wait(bars.dq_free, ph ^ 1u)) break;
-    issue_dP(it);
-    if (!wait(bars.pds_full[0], ph)) break;
+    const uint32_t acc0 = first_in_seg ? 0u : 1u;
+    // the first dV / dK of a run overwrite the accumulators: the reducers
+    // must have flushed the previous run
     if (first_in_seg && seg_done > 0 && !wait(bars.dkv_free, uint32_t((seg_done - 1) & 1)))
       break;
-    issue_dkdv(it, 0, first_in_seg ? 0u : 1u);
-    if (!wait(bars.pds_full[1], ph)) break;
-    issue_dkdv(it, 1, 1u);
-    umma_commit(smem_u32(&bars.dk_done));
-    umma_commit(smem_u32(&bars.dv_done));
-    // dQ^T is written over dS^T: dK must have read it.
-    if (!wait(bars.dk_done, ph)) break;
+    if (!wait(bars.p_ready[0], ph)) break;
+    issue_dv(it, 0, acc0);
+    if (!wait(bars.p_ready[1], ph)) break;
+    issue_dv(it, 1, 1u);
+    if (!wait(bars.ds_ready[0], ph)) break;
+    issue_dk(it, 0, acc0);
+    if (!wait(bars.ds_ready[1], ph)) break;
+    issue_dk(it, 1, 1u);
+    umma_commit(smem_u32(&bars.pt_free));
+    // dQ^T into the dP^T columns, which the compute warps have read
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ss(tmem + kTmDQ, mK + mstep(kk), mDS + mstep(kk), idMM, kk > 0);
     umma_commit(smem_u32(&bars.dq_full));
     first_in_seg = false;
+    const bool seg_end = it + 1 == my_n || next_kv != cur_kv;
+    if (seg_end) umma_commit(smem_u32(&bars.seg_done));  // dV / dK of the run are final
     if (it + 1 < my_n) {
-      if (next_kv != cur_kv) {
+      if (seg_end) {
         ++seg_done;
         umma_commit(smem_u32(&bars.kv_empty));
         if (!wait(bars.kv_full, uint32_t(kv_loads & 1))) break;
@@ -249,10 +273,14 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
         cur_kv = next_kv;
         first_in_seg = true;
       }
-      // S^T(it+1) overwrites P^T(it): dV(it) must have read it.
-      if (!wait(bars.dv_done, ph)) break;
+      // S^T(it+1) overwrites P^T(it) and dS^T(it): dV(it) and dK(it) must
+      // have read them.
+      if (!wait(bars.pt_free, ph)) break;
       if (!wait(bars.qdo_full[(it + 1) & 1], uint32_t(((it + 1) >> 1) & 1))) break;
       issue_S(it + 1);
+      // dP^T(it+1) overwrites dQ^T(it): the reducers must have read it.
+      if (!wait(bars.dq_free, ph)) break;
+      issue_dP(it + 1);
     }
     next_kv = next2_kv;
   }
@@ -263,20 +291,23 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
 // Warp roles (448 threads):
 //   0      TMA producer: K/V per block run, Q/dO per task (two stages)
 //   1      MMA issuer, TMEM owner
-//   2-9    compute: P^T, dS^T; warps 2-5 own q-rows [0,64), warps 6-9 [64,128)
-//   10-13  reduce: dQ^T -> pool (thread = head dim), dV / dK flush
+//   2-9    compute: P^T, dS^T (TMEM) and dS (shared memory), then dQ^T read
+//          out of TMEM and added to the pool with packed atomics; warps 2-5
+//          own q-rows [0,64), warps 6-9 [64,128)
+//   10-13  dV / dK flush at the end of a run (thread = key)
 template <int ACC>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_main(const __grid_constant__ BwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapK,
-               const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDQ) {
+               const __grid_constant__ CUtensorMap mapV) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, skip_sh;
+  // Column (q-row) scalars of the current task.
   __shared__ __align__(16) float s_nlse2[128];  // -LSE * log2(e)
   __shared__ __align__(16) float s_delta[128];
-  __shared__ __align__(16) int8_t s_jlim[128];
+  __shared__ __align__(16) int8_t s_jlim[128];  // last visible key, -1 for padding
   __shared__ int s_wfull[4];  // per lane quadrant: every column sees all 128 keys
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -294,14 +325,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&bars.qdo_full[i]), 1);
       mbar_init(smem_u32(&bars.qdo_empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars.sdp_full), 1);
-    mbar_init(smem_u32(&bars.pds_full[0]), 128);
-    mbar_init(smem_u32(&bars.pds_full[1]), 128);
-    mbar_init(smem_u32(&bars.dk_done), 1);
-    mbar_init(smem_u32(&bars.dv_done), 1);
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.dp_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.p_ready[i]), 128);
+      mbar_init(smem_u32(&bars.ds_ready[i]), 128);
+    }
+    mbar_init(smem_u32(&bars.pt_free), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
-    mbar_init(smem_u32(&bars.dq_free), 128);
+    mbar_init(smem_u32(&bars.dq_free), 256);
+    mbar_init(smem_u32(&bars.seg_done), 1);
     mbar_init(smem_u32(&bars.dkv_free), 128);
+    mbar_init(smem_u32(&bars.cols), 256);
     mbar_init(smem_u32(&bars.fin), 1);
     fence_mbar_init();
   }
@@ -387,200 +422,229 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---------------- MMA issuer
     if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, my_n, chunk, abort_flag);
   } else if (warp < 10) {
-    // ---------------- compute: P^T, dS^T (thread = key; half = block of 64 q-rows)
+    // ---------------- compute (thread = TMEM lane; half = block of 64 q-rows)
+    // Phase 1 (after S^T; thread = key): P = 2^(S^T c2 - LSE log2 e), masked
+    // after the column's query on diagonal blocks, as bf16 pairs into TMEM
+    // (A operand of dV) and kept in registers.  Phase 2 (after dP^T):
+    // dS = P (dP^T - delta) as bf16 into TMEM (A operand of dK) and into the
+    // shared-memory dS tile (row = key, 128-byte swizzle; B operand of dQ^T).
+    // Phase 3 (after dQ^T; thread = head dim): dQ^T read out, scaled and
+    // added to the head-pair-interleaved pool with packed atomics.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int r = quad * 32 + lane;  // key within the block = TMEM lane
+    const int r = quad * 32 + lane;  // key (phases 1, 2) / head dim (phase 3) = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    // One 16-column sub-chunk (q-rows cb .. cb+15, cb = 64 half + 16 sc), in
-    // fp32 pairs:  P = 2^(S^T c2 - LSE log2 e),  dS = P (dP^T - delta).
-    auto sub_chunk = [&](int sc, const uint32_t (&sv)[16], const uint32_t (&dv)[16], bool full) {
-      const int cb = half * 64 + sc * 16;
-      const uint4* l4 = reinterpret_cast<const uint4*>(s_nlse2 + cb);
-      const uint4* d4 = reinterpret_cast<const uint4*>(s_delta + cb);
-      const uint4 jw = *reinterpret_cast<const uint4*>(s_jlim + cb);
-      const uint32_t jwa[4] = {jw.x, jw.y, jw.z, jw.w};
-      uint64_t nl[8], dl[8];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 x = l4[q4], y = d4[q4];
-        nl[2 * q4] = f2_pack(x.x, x.y);
-        nl[2 * q4 + 1] = f2_pack(x.z, x.w);
-        dl[2 * q4] = f2_pack(y.x, y.y);
-        dl[2 * q4 + 1] = f2_pack(y.z, y.w);
-      }
-      const uint64_t cc = f2_pack(__float_as_uint(prm.c2), __float_as_uint(prm.c2));
-      uint32_t pp[8], pd[8];
-#pragma unroll
-      for (int jp = 0; jp < 8; ++jp) {
-        const uint64_t x2 = f2_fma(f2_pack(sv[2 * jp], sv[2 * jp + 1]), cc, nl[jp]);
-        float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
-        if (!full) {  // keys after the column's query (diagonal block) get P = 0
-          const int j = 2 * jp;
-          const int jl0 = int(int8_t((jwa[j >> 2] >> (8 * (j & 3))) & 0xFF));
-          const int jl1 = int(int8_t((jwa[j >> 2] >> (8 * ((j + 1) & 3))) & 0xFF));
-          p0 = r <= jl0 ? p0 : 0.f;
-          p1 = r <= jl1 ? p1 : 0.f;
-        }
-        const uint64_t p2 = f2_pack(__float_as_uint(p0), __float_as_uint(p1));
-        const uint64_t ds = f2_mul(p2, f2_sub(f2_pack(dv[2 * jp], dv[2 * jp + 1]), dl[jp]));
-        pp[jp] = pack_bf16x2(p0, p1);
-        pd[jp] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
-      }
-      tmem_st8_nc(tmem + lane_base + kTmP + half * 64 + sc * 8, pp);
-      tmem_st8_nc(tmem + lane_base + kTmDST + half * 64 + sc * 8, pd);
-      // dS (B operand of dQ^T, MN-major): tile row = key r, cols = q-rows
-      const uint32_t rowb = sbase + kSmDS + half * 16384 + r * 128;
-      const uint32_t c0 = uint32_t((2 * sc) ^ (r & 7)) * 16;
-      const uint32_t c1 = uint32_t((2 * sc + 1) ^ (r & 7)) * 16;
-      st_shared_v4_nc(rowb + c0, pd[0], pd[1], pd[2], pd[3]);
-      st_shared_v4_nc(rowb + c1, pd[4], pd[5], pd[6], pd[7]);
-    };
-    // Column scalars of task it+1 are loaded while task it is computed, in
-    // two steps so no load result is consumed right after it is issued: the
-    // column's token at the top of task it, its LSE / delta mid-way.
+    const uint32_t cS = tmem + lane_base + kTmS + half * 64;
+    const uint32_t cD = tmem + lane_base + kTmDP + half * 64;
+    const uint32_t cQ = tmem + lane_base + kTmDQ + half * 64;
+    const uint32_t rowb = sbase + kSmDS + half * 16384 + r * 128;
+    const uint64_t cc = f2_pack(__float_as_uint(prm.c2), __float_as_uint(prm.c2));
+    // Half 0 also loads the column scalars of the next task: thread r owns
+    // column r (query r / 16 of the task, head r % 16).
     const int qi = r >> 4, hh = r & 15;
-    int4 rec1 = task_rec(tasks, 1, my_n, chunk);
-    // (raw LSE: scaling it where it is loaded would wait for the load)
-    float clse = 0.f, cdl = 0.f;  // current task's column values
-    int cjl = -1;
+    auto col_row = [&](const TaskView& tv, int32_t tok) {
+      return int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
+    };
+    auto col_jlim = [&](const TaskView& tv, int32_t tok) {
+      return qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
+    };
+    auto put_cols = [&](float lse, float dl, int jl) {
+      s_nlse2[r] = -lse * kLog2e;
+      s_delta[r] = dl;
+      s_jlim[r] = int8_t(jl);
+      const bool wf = __all_sync(0xffffffffu, jl == kBlock - 1);
+      if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
+    };
+    int4 rec0 = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    int32_t tok1 = 0;
     if (half == 0 && my_n > 0) {
-      const TaskView tv = decode_task(task_rec(tasks, 0, my_n, chunk));
+      const TaskView tv = decode_task(rec0);
       const int32_t tok = task_token(p.col, tv, qi);
-      const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      cjl = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
-      clse = prm.lse[grow];
-      cdl = prm.delta[grow];
+      const int64_t grow = col_row(tv, tok);
+      put_cols(prm.lse[grow], prm.delta[grow], col_jlim(tv, tok));
+      if (my_n > 1) tok1 = task_token(p.col, decode_task(rec1), qi);
     }
-    for (int64_t it = 0; it < my_n; ++it) {
-      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
-      int32_t ntok = 0;
-      if (half == 0 && it + 1 < my_n) ntok = task_token(p.col, decode_task(rec1), qi);
-      named_bar_sync(1, 256);  // previous task's columns fully consumed
-      if (half == 0) {
-        s_nlse2[r] = -clse * kLog2e;
-        s_delta[r] = cdl;
-        s_jlim[r] = int8_t(cjl);
-        const bool wf = __all_sync(0xffffffffu, cjl == kBlock - 1);
-        if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
-      }
-      named_bar_sync(1, 256);
-      if (!mbar_wait_warp(smem_u32(&bars.sdp_full), uint32_t(it & 1), abort_flag)) break;
-      tc_fence_after();
-      const bool full = s_wfull[0] & s_wfull[1] & s_wfull[2] & s_wfull[3];
-      const uint32_t cS = tmem + lane_base + kTmS + half * 64;
-      const uint32_t cD = tmem + lane_base + kTmDP + half * 64;
-      uint32_t sA[16], dA[16], sB[16], dB[16];
-      tmem_ld16(cS, sA);
-      tmem_ld16(cD, dA);
-      tmem_ld_wait();
-#pragma unroll 1
-      for (int sp = 0; sp < 2; ++sp) {
-        const int sc0 = 2 * sp, sc1 = 2 * sp + 1;
-        tmem_ld16(cS + sc1 * 16, sB);
-        tmem_ld16(cD + sc1 * 16, dB);
-        sub_chunk(sc0, sA, dA, full);
-        tmem_ld_wait();
-        if (sp < 1) {
-          tmem_ld16(cS + (sc1 + 1) * 16, sA);
-          tmem_ld16(cD + (sc1 + 1) * 16, dA);
-          if (half == 0 && it + 1 < my_n) {  // next task's column values
-            const TaskView tn = decode_task(rec1);
-            const int64_t grow = int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh;
-            cjl = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
-            clse = prm.lse[grow];
-            cdl = prm.delta[grow];
-          }
+    // Column scalars of a task are published through the `cols` barrier
+    // (phase 0: task 0; phase it + 1: task it + 1).  Half 0 overwrites them
+    // once both halves have finished phase 2 of task it (ds_ready).
+    mbar_arrive(smem_u32(&bars.cols));
+    bool cols_ok = mbar_wait_warp(smem_u32(&bars.cols), 0u, abort_flag);
+    uint32_t pk[32];  // P of this thread's key for the half's 64 q-rows, bf16 pairs
+    // ---- phase 1 over the half's 64 columns (S^T values in a0, a1)
+    auto phase1 = [&](auto full_t, const uint32_t (&a0)[32], const uint32_t (&a1)[32],
+                      const float* nl, const int8_t* jl) {
+      constexpr bool kFull = decltype(full_t)::value;
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const uint32_t* v = q4 < 8 ? &a0[4 * q4] : &a1[4 * (q4 - 8)];
+        const uint4 x = *reinterpret_cast<const uint4*>(nl + 4 * q4);
+        const uint64_t e0 = f2_fma(f2_pack(v[0], v[1]), cc, f2_pack(x.x, x.y));
+        const uint64_t e1 = f2_fma(f2_pack(v[2], v[3]), cc, f2_pack(x.z, x.w));
+        float p0 = fast_exp2(f2_lo(e0)), p1 = fast_exp2(f2_hi(e0));
+        float p2 = fast_exp2(f2_lo(e1)), p3 = fast_exp2(f2_hi(e1));
+        if constexpr (!kFull) {  // keys after the column's query get P = 0
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(jl + 4 * q4);
+          p0 = r <= int(int8_t(w & 0xFF)) ? p0 : 0.f;
+          p1 = r <= int(int8_t((w >> 8) & 0xFF)) ? p1 : 0.f;
+          p2 = r <= int(int8_t((w >> 16) & 0xFF)) ? p2 : 0.f;
+          p3 = r <= int(int8_t(w >> 24)) ? p3 : 0.f;
         }
-        sub_chunk(sc1, sB, dB, full);
-        tmem_ld_wait();
+        pk[2 * q4] = pack_bf16x2(p0, p1);
+        pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
       }
+    };
+    for (int64_t it = 0; cols_ok && it < my_n; ++it) {
+      const uint32_t ph = uint32_t(it & 1);
+      const int st = int(it & 1);
+      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      // the next task's column scalars: issued now, stored after phase 2
+      float lse1 = 0.f, dl1 = 0.f;
+      int jl1 = -1;
+      if (half == 0 && it + 1 < my_n) {
+        const TaskView tv1 = decode_task(rec1);
+        const int64_t grow = col_row(tv1, tok1);
+        lse1 = prm.lse[grow];
+        dl1 = prm.delta[grow];
+        jl1 = col_jlim(tv1, tok1);
+      }
+      const bool full = (s_wfull[0] & s_wfull[1] & s_wfull[2] & s_wfull[3]) != 0;
+      const float* nl = &s_nlse2[half * 64];
+      const float* dlt = &s_delta[half * 64];
+      const int8_t* jl = &s_jlim[half * 64];
+      // ---- phase 1
+      if (!mbar_wait_warp(smem_u32(&bars.s_full), ph, abort_flag)) break;
+      tc_fence_after();
+      {
+        uint32_t a0[32], a1[32];
+        tmem_ld32(cS, a0);
+        tmem_ld32(cS + 32, a1);
+        tmem_ld_wait();
+        reg_fence32(a0);
+        reg_fence32(a1);
+        if (full)
+          phase1(std::true_type{}, a0, a1, nl, jl);
+        else
+          phase1(std::false_type{}, a0, a1, nl, jl);
+      }
+      tmem_st32_nc(cS + kTmP, pk);
       tmem_st_wait();
       tc_fence_before();
+      mbar_arrive(smem_u32(&bars.p_ready[half]));
+      int32_t tok2 = 0;
+      if (half == 0 && it + 2 < my_n) tok2 = task_token(p.col, decode_task(rec2), qi);
+      // tokens of the half's four queries, for the dQ atomics of phase 3
+      const TaskView tv0 = decode_task(rec0);
+      int32_t tq[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tq[k] = task_token(p.col, tv0, 4 * half + k);
+      // ---- phase 2
+      if (!mbar_wait_warp(smem_u32(&bars.dp_full), ph, abort_flag)) break;
+      tc_fence_after();
+      {
+        // 16 q-rows at a time; the second 32 columns of dP^T are loaded while
+        // the first are processed
+        auto chunk = [&](int sc, const uint32_t* v) {
+          uint32_t pd[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int q4 = 4 * sc + q;
+            const uint4 y = *reinterpret_cast<const uint4*>(dlt + 4 * q4);
+            const uint32_t w0 = pk[2 * q4], w1 = pk[2 * q4 + 1];
+            const uint64_t da = f2_mul(f2_pack(w0 << 16, w0 & 0xFFFF0000u),
+                                       f2_sub(f2_pack(v[4 * q], v[4 * q + 1]), f2_pack(y.x, y.y)));
+            const uint64_t db = f2_mul(f2_pack(w1 << 16, w1 & 0xFFFF0000u),
+                                       f2_sub(f2_pack(v[4 * q + 2], v[4 * q + 3]), f2_pack(y.z, y.w)));
+            pd[2 * q] = pack_bf16x2(f2_lo(da), f2_hi(da));
+            pd[2 * q + 1] = pack_bf16x2(f2_lo(db), f2_hi(db));
+          }
+          tmem_st8_nc(cS + kTmDS + sc * 8, pd);
+          // dS tile row = key r, columns = q-rows: 16-byte chunks 2 sc, 2 sc + 1
+          // of this half, swizzled by (r & 7)
+          st_shared_v4_nc(rowb + uint32_t((2 * sc) ^ (r & 7)) * 16, pd[0], pd[1], pd[2], pd[3]);
+          st_shared_v4_nc(rowb + uint32_t((2 * sc + 1) ^ (r & 7)) * 16, pd[4], pd[5], pd[6],
+                          pd[7]);
+        };
+        uint32_t b[32];
+        tmem_ld32(cD, b);
+        tmem_ld_wait();
+        reg_fence32(b);
+        chunk(0, &b[0]);
+        chunk(1, &b[16]);
+        tmem_ld32(cD + 32, b);
+        tmem_ld_wait();
+        reg_fence32(b);
+        chunk(2, &b[0]);
+        chunk(3, &b[16]);
+      }
+      tmem_st_wait();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bars.pds_full[half]));
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.ds_ready[half]));
+      if (half == 0 && it + 1 < my_n) {
+        if (!mbar_wait_warp(smem_u32(&bars.ds_ready[0]), ph, abort_flag) ||
+            !mbar_wait_warp(smem_u32(&bars.ds_ready[1]), ph, abort_flag))
+          break;
+        put_cols(lse1, dl1, jl1);
+      }
+      // next task's column scalars visible, this task's consumed
+      mbar_arrive(smem_u32(&bars.cols));
+      if (!mbar_wait_warp(smem_u32(&bars.cols), ph ^ 1u, abort_flag)) break;
+      // ---- phase 3: dQ^T (lane = head dim d = r, columns = the half's q-rows)
+      if (!mbar_wait_warp(smem_u32(&bars.dq_full), ph, abort_flag)) break;
+      tc_fence_after();
+      // every MMA of the task is complete: its Q / dO stage is free
+      if (warp == 2 && lane == 0) mbar_arrive(smem_u32(&bars.qdo_empty[st]));
+      {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(cQ, v0);
+        tmem_ld32(cQ + 32, v1);
+        tmem_ld_wait();
+        reg_fence32(v0);
+        reg_fence32(v1);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_free));  // dP^T(it+1) may overwrite dQ^T(it)
+        // q-rows 16 k + 2 m, 16 k + 2 m + 1 are heads 2 m, 2 m + 1 of query
+        // 4 half + k: one pool word (two 16-bit or two fp32 values) per head
+        // dimension; lanes hold consecutive head dimensions.
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (4 * half + k >= tv0.nq) continue;
+          const int64_t pr0 = int64_t(tq[k]) * (kQHeads / 2) + tv0.g * (kHeadsPerGroup / 2);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int j = 16 * k + 2 * m;
+            const float a = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]) * prm.scale;
+            const float b = __uint_as_float(j < 32 ? v0[j + 1] : v1[j - 31]) * prm.scale;
+            const int64_t e = ((pr0 + m) * kHeadDim + r) * 2;
+            if (ACC == MSA_DQ_ACCUM_F32)
+              red_add_v2_f32(static_cast<float*>(prm.dq_pool) + e, a, b);
+            else if (ACC == MSA_DQ_ACCUM_BF16)
+              red_add_bf16x2(static_cast<__nv_bfloat16*>(prm.dq_pool) + e, pack_bf16x2(a, b));
+            else
+              red_add_f16x2(static_cast<__half*>(prm.dq_pool) + e, pack_f16x2(a, b));
+          }
+        }
+      }
+      rec0 = rec1;
       rec1 = rec2;
+      tok1 = tok2;
     }
   } else {
-    // ---------------- reduce: dQ^T -> pool (thread = head dim), dV / dK flush
+    // ---------------- dV / dK flush at the end of each run (thread = key)
     const int quad = warp & 3;
-    const int d = quad * 32 + lane;  // head dim = TMEM lane (dQ^T); key for dV / dK
+    const int key = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    const bool odd = lane & 1;
-    const bool issuer = (warp == 10 && lane == 0);
     int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    int64_t nseg = 0;
     for (int64_t it = 0; it < my_n; ++it) {
       const TaskView tv = decode_task(rec);
       const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
-      int32_t tok[kTaskQueries];
-#pragma unroll
-      for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = task_token(p.col, tv, qi);
-      if (!mbar_wait_warp(smem_u32(&bars.dq_full), uint32_t(it & 1), abort_flag)) break;
-      tc_fence_after();
-      const int64_t gb = int64_t(tv.g) * kHeadsPerGroup;
-      const int st = int(it & 1);
-      // dq_full(it) means every MMA of the task is complete, so the task's
-      // Q tile is free: stage the 16-bit dQ tile row-major in it, then one
-      // thread adds it to the pool with one bulk tensor reduction per query
-      // (16 heads x 128 dims = 4 KB) and hands the Q/dO stage back to the
-      // producer.  Even lanes write (row j, dims d, d+1), odd lanes (row j+1,
-      // dims d-1, d).
-      const uint32_t stage_base = sbase + kSmQ + st * kTileBytes;
-      const uint32_t stage = stage_base + uint32_t(odd ? 256 + 2 * (d - 1) : 2 * d);
-      auto consume = [&](const uint32_t (&v)[64], int j0) {
-        if (ACC == MSA_DQ_ACCUM_F32) {
-          float* pool = static_cast<float*>(prm.dq_pool) + d;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int jj = j0 + j;
-            if ((jj >> 4) < tv.nq)
-              red_add_f32(pool + ((int64_t(tok[jj >> 4]) * kQHeads + gb + (jj & 15)) * kHeadDim),
-                          __uint_as_float(v[j]) * prm.scale);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float a = __uint_as_float(v[j]) * prm.scale;
-            const float b = __uint_as_float(v[j + 1]) * prm.scale;
-            const float x = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-            const float lo = odd ? x : a, hi = odd ? b : x;
-            const uint32_t w2 =
-                ACC == MSA_DQ_ACCUM_F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
-            const int jj = j0 + j;
-            st_shared_b32(stage + (jj >> 4) * 4096 + (jj & 15) * 256, w2);
-          }
-        }
-      };
-      uint32_t v[64];
-      tmem_ld32(tmem + lane_base + kTmDQ + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tmem + lane_base + kTmDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld_wait();
-      consume(v, 0);
-      tmem_ld32(tmem + lane_base + kTmDQ + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tmem + lane_base + kTmDQ + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.dq_free));
-      consume(v, 64);
-      if (ACC != MSA_DQ_ACCUM_F32) {
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (issuer) {
-          for (int qi = 0; qi < tv.nq; ++qi)
-            for (unsigned h0 = 0; h0 < unsigned(kHeadsPerGroup); h0 += kDqReduceRows)
-              tma_reduce_add_2d(&mapDQ, stage_base + qi * 4096 + h0 * 256, 0,
-                                tok[qi] * kQHeads + tv.g * kHeadsPerGroup + int(h0));
-          bulk_commit();
-          bulk_wait_read0();
-          mbar_arrive(smem_u32(&bars.qdo_empty[st]));
-        }
-      } else if (issuer) {
-        mbar_arrive(smem_u32(&bars.qdo_empty[st]));
-      }
       const bool seg_end = (it + 1 == my_n) || rec1.w != tv.sub;
       if (seg_end) {
-        // dq_full(it) follows dv_done / dk_done(it): dV / dK of the run are final.
-        const int key = d;
+        // seg_done follows the run's last dV / dK MMAs: the accumulators are final
+        if (!mbar_wait_warp(smem_u32(&bars.seg_done), uint32_t(nseg & 1), abort_flag)) break;
+        ++nseg;
+        tc_fence_after();
         const bool key_valid = key < tv.key_len;
         const int64_t krow = (int64_t(tv.key_start) + key) * kKVHeads + tv.g;
 #pragma unroll 1
@@ -609,7 +673,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       rec = rec1;
       rec1 = rec2;
     }
-    if (issuer) bulk_wait0();  // bulk reductions complete before the CTA exits
   }
 
   if (threadIdx.x == 0 && abort_sh) raise_status(p.header, MSA_ERR_TIMEOUT);
@@ -619,50 +682,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------ bwd_finalize
-// Pools -> bf16 outputs, 8 elements per thread.
+// Pools -> bf16 outputs.  dQ: one thread per (token, head pair, 8 head
+// dimensions) reads the 16 interleaved pool values and writes 8 dims of each
+// head; dK / dV: 8 elements per thread.
 __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq_pool,
                                                       const float* dk_pool, const float* dv_pool,
                                                       __nv_bfloat16* dq, __nv_bfloat16* dk,
                                                       __nv_bfloat16* dv) {
   if (plan_failed(p.header)) return;
-  const int64_t nq8 = p.T * kQHeads * kHeadDim / 8, nk8 = p.T * kKVHeads * kHeadDim / 8;
+  const int64_t nq = p.T * (kQHeads / 2) * (kHeadDim / 8);
+  const int64_t nk8 = p.T * kKVHeads * kHeadDim / 8;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq8 + 2 * nk8;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq + 2 * nk8;
        i += stride) {
-    float f[8];
-    uint4* dst;
-    if (i < nq8) {
+    if (i < nq) {
+      const int64_t pr = i >> 4;  // token * 32 + head pair
+      const int d0 = int(i & 15) * 8;
+      float f0[8], f1[8];  // heads 2 hp and 2 hp + 1
       if (p.dq_accum == MSA_DQ_ACCUM_F32) {
-        const float4 a = reinterpret_cast<const float4*>(dq_pool)[2 * i];
-        const float4 b = reinterpret_cast<const float4*>(dq_pool)[2 * i + 1];
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-      } else {
-        const uint4 a = reinterpret_cast<const uint4*>(dq_pool)[i];
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+        const float4* src = reinterpret_cast<const float4*>(
+            static_cast<const float*>(dq_pool) + (pr * kHeadDim + d0) * 2);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int u = 0; u < 4; ++u) {
+          const float4 a = src[u];
+          f0[2 * u] = a.x; f1[2 * u] = a.y; f0[2 * u + 1] = a.z; f1[2 * u + 1] = a.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(dq_pool) + (pr * kHeadDim + d0) * 2);
+        const uint4 a = src[0], b = src[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
           if (p.dq_accum == MSA_DQ_ACCUM_F16) {
-            f[2 * e] = f16_lo(w[e]);
-            f[2 * e + 1] = f16_hi(w[e]);
+            f0[e] = f16_lo(w[e]);
+            f1[e] = f16_hi(w[e]);
           } else {
-            f[2 * e] = bf16_lo(w[e]);
-            f[2 * e + 1] = bf16_hi(w[e]);
+            f0[e] = bf16_lo(w[e]);
+            f1[e] = bf16_hi(w[e]);
           }
         }
       }
-      dst = reinterpret_cast<uint4*>(dq) + i;
+      __nv_bfloat16* o = dq + (2 * pr) * kHeadDim + d0;
+      *reinterpret_cast<uint4*>(o) =
+          make_uint4(pack_bf16x2(f0[0], f0[1]), pack_bf16x2(f0[2], f0[3]),
+                     pack_bf16x2(f0[4], f0[5]), pack_bf16x2(f0[6], f0[7]));
+      *reinterpret_cast<uint4*>(o + kHeadDim) =
+          make_uint4(pack_bf16x2(f1[0], f1[1]), pack_bf16x2(f1[2], f1[3]),
+                     pack_bf16x2(f1[4], f1[5]), pack_bf16x2(f1[6], f1[7]));
     } else {
-      const int64_t j = i < nq8 + nk8 ? i - nq8 : i - nq8 - nk8;
-      const float* src = i < nq8 + nk8 ? dk_pool : dv_pool;
+      const int64_t j = i < nq + nk8 ? i - nq : i - nq - nk8;
+      const float* src = i < nq + nk8 ? dk_pool : dv_pool;
       const float4 a = reinterpret_cast<const float4*>(src)[2 * j];
       const float4 b = reinterpret_cast<const float4*>(src)[2 * j + 1];
-      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-      f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-      dst = reinterpret_cast<uint4*>(i < nq8 + nk8 ? dk : dv) + j;
+      *(reinterpret_cast<uint4*>(i < nq + nk8 ? dk : dv) + j) =
+          make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                     pack_bf16x2(b.z, b.w));
     }
-    *dst = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
   }
 }
 
@@ -670,7 +746,6 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
 
 CUresult make_map_rows(CUtensorMap* m, const void* base, int64_t rows);
 CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T);
-CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows, bool bf16);
 int device_sm_count();
 
 size_t backward_workspace_bytes(const msa_plan& p) { return bwd_layout(p).total; }
@@ -685,15 +760,10 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   float* dk_pool = reinterpret_cast<float*>(w + L.off_dk);
   float* dv_pool = reinterpret_cast<float*>(w + L.off_dv);
 
-  CUtensorMap mQ, mDO, mK, mV, mDQ;
-  memset(&mDQ, 0, sizeof mDQ);
+  CUtensorMap mQ, mDO, mK, mV;
   if (make_map_rows(&mQ, q, p.T * kQHeads) != CUDA_SUCCESS ||
       make_map_rows(&mDO, dout, p.T * kQHeads) != CUDA_SUCCESS ||
       make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  if (p.dq_accum != MSA_DQ_ACCUM_F32 &&
-      make_map_pool16(&mDQ, dq_pool, p.T * kQHeads, p.dq_accum == MSA_DQ_ACCUM_BF16) !=
-          CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   const int64_t rows = p.T * kQHeads;
@@ -721,11 +791,11 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   launch_begin("bwd_main", s);
   const unsigned grid = unsigned(device_sm_count());
   if (p.dq_accum == MSA_DQ_ACCUM_F32)
-    k_bwd_main<MSA_DQ_ACCUM_F32><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
+    k_bwd_main<MSA_DQ_ACCUM_F32><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
   else if (p.dq_accum == MSA_DQ_ACCUM_BF16)
-    k_bwd_main<MSA_DQ_ACCUM_BF16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
+    k_bwd_main<MSA_DQ_ACCUM_BF16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
   else
-    k_bwd_main<MSA_DQ_ACCUM_F16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV, mDQ);
+    k_bwd_main<MSA_DQ_ACCUM_F16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
   launch_end("bwd_main", s);
   launch_begin("bwd_finalize", s);
   k_bwd_finalize<<<unsigned(device_sm_count() * 8), 256, 0, s>>>(

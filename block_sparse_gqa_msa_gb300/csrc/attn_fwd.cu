@@ -201,16 +201,18 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
 //         fp16 written over the row's S columns, row sum; warps 2-5 take the
 //         even tasks (TMEM stage 0), warps 6-9 the odd ones (stage 1)
 //   10-13 epilogue (thread = tile row): O_part * exp(m - M) staged in shared
-//         memory and added to the fp32 pool by one 512 B bulk reduction per
-//         row; row sums by atomics
+//         memory and added to the fp32 pool by bulk tensor reductions (four
+//         2 KB boxes per query, issued by one lane per warp); row sums by
+//         atomics
 //   14    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
 // TMEM: S (and P over its first 64 columns) in [0,128) / [128,256), O_part in
 // [256,384) / [384,512), two stages each.
 constexpr int kFwdThreads = 480;
 constexpr uint32_t kTileBytes = 32768;
 constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
-constexpr uint32_t kStageRowBytes = 528;  // 512 B of data + 16 B pad
-constexpr uint32_t kStageBytes = 128 * kStageRowBytes;
+// Epilogue staging: per query of the tile, four 2 KB boxes (16 heads x 32
+// columns, fp32, 128-byte swizzle) - the boxes of the pool's tensor map.
+constexpr uint32_t kStageBytes = kTaskQueries * 8192;
 constexpr uint32_t kFwdSmem = kSmStage + kStageBytes + 1024;
 
 struct FwdBars {
@@ -246,6 +248,93 @@ __device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n
 }
 __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
+}
+
+// Softmax of one tile row held in TMEM columns [cs, cs + 128) of the
+// thread's lane: keys after jmax are excluded when MASK (diagonal and partial
+// blocks, padded queries with jmax = -1).
+template <bool MASK>
+__device__ __forceinline__ float tile_row_max(uint32_t cs, int jmax) {
+  float m[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) m[e] = -INFINITY;
+  auto reduce = [&](const uint32_t (&r)[16], int lim) {  // lim = jmax - first column
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      float x0 = __uint_as_float(r[j]), x1 = __uint_as_float(r[j + 1]);
+      if (MASK) {
+        x0 = j <= lim ? x0 : -INFINITY;
+        x1 = j + 1 <= lim ? x1 : -INFINITY;
+      }
+      m[(j >> 1) & 3] = fmax3(m[(j >> 1) & 3], x0, x1);
+    }
+  };
+  uint32_t r0[16], r1[16];
+  tmem_ld16(cs, r0);
+  tmem_ld_wait();
+  reg_fence16(r0);
+  // 16-column chunks 2i (r0) and 2i+1 (r1); the next chunk loads while the
+  // current one is reduced
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    tmem_ld16(cs + 32 * i + 16, r1);
+    reduce(r0, jmax - 32 * i);
+    tmem_ld_wait();
+    reg_fence16(r1);
+    if (i < 3) tmem_ld16(cs + 32 * i + 32, r0);
+    reduce(r1, jmax - 32 * i - 16);
+    if (i < 3) {
+      tmem_ld_wait();
+      reg_fence16(r0);
+    }
+  }
+  return fmaxf(fmax3(m[0], m[1], m[2]), m[3]);
+}
+
+// P = 2^(s c2 - mxc) written as fp16 pairs over the columns already read
+// (columns [cs + 8c, cs + 8c + 8) after reading [cs + 16c, cs + 16c + 16));
+// the next 16 columns are loaded while the current ones are exponentiated.
+// Returns the row sum of the fp32 values.
+template <bool MASK>
+__device__ __forceinline__ float tile_row_exp(uint32_t cs, int jmax, float c2, float mxc) {
+  const uint64_t cc = f2_pack(__float_as_uint(c2), __float_as_uint(c2));
+  const uint64_t nm = f2_pack(__float_as_uint(-mxc), __float_as_uint(-mxc));
+  uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
+  auto expo = [&](const uint32_t (&r)[16], int lim, uint32_t dst) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const uint64_t x2 = f2_fma(f2_pack(r[j], r[j + 1]), cc, nm);
+      float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
+      if (MASK) {
+        p0 = j <= lim ? p0 : 0.f;
+        p1 = j + 1 <= lim ? p1 : 0.f;
+      }
+      ls[(j >> 1) & 3] =
+          f2_add(ls[(j >> 1) & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+      pk[j >> 1] = pack_f16x2(p0, p1);
+    }
+    tmem_st8_nc(dst, pk);
+  };
+  uint32_t r0[16], r1[16];
+  tmem_ld16(cs, r0);
+  tmem_ld_wait();
+  reg_fence16(r0);
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    tmem_ld16(cs + 32 * i + 16, r1);
+    expo(r0, jmax - 32 * i, cs + 16 * i);
+    tmem_ld_wait();
+    reg_fence16(r1);
+    if (i < 3) tmem_ld16(cs + 32 * i + 32, r0);
+    expo(r1, jmax - 32 * i - 16, cs + 16 * i + 8);
+    if (i < 3) {
+      tmem_ld_wait();
+      reg_fence16(r0);
+    }
+  }
+  const uint64_t s2 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
+  return f2_lo(s2) + f2_hi(s2);
 }
 
 // MMA issuer of k_fwd_main (one thread).  A function of its own so its few
@@ -322,7 +411,8 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_main(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
-               const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV) {
+               const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+               const __grid_constant__ CUtensorMap mapPool) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdBars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -484,56 +574,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       tc_fence_after();
       const uint32_t cs = tmem + lane_base + st * 128;
+      // A warp whose 32 rows all see the whole key block (every tile that is
+      // not on a document's diagonal or last partial block) skips the masks.
+      const bool full = __all_sync(0xffffffffu, jmax == kBlock - 1);
       // pass 1: the tile row's maximum over visible keys (raw scores)
-      // (eight independent running maxima keep the dependency chains short)
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      {
-        uint32_t a[32], b[32];
-        tmem_ld32(cs, a);
-        tmem_ld32(cs + 32, b);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(a[j]));
-          if (32 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(b[j]));
-        }
-        tmem_ld32(cs + 64, a);
-        tmem_ld32(cs + 96, b);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (64 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(a[j]));
-          if (96 + j <= jmax) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(b[j]));
-        }
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx = full ? tile_row_max<false>(cs, jmax) : tile_row_max<true>(cs, jmax);
       const float mxc = (jmax >= 0) ? mx * prm.c2 : 0.f;
-      // pass 2: P = exp(s - m) as fp16 pairs over S columns [16c, 16c+16)
-      // (columns already read); row sum of the fp32 values
-      float ls8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ls8[e] = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(cs + c * 32, r);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int k0 = c * 32 + j;
-          const float x0 = (k0 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j]), prm.c2, -mxc)) : 0.f;
-          const float x1 =
-              (k0 + 1 <= jmax) ? fast_exp2(fmaf(__uint_as_float(r[j + 1]), prm.c2, -mxc)) : 0.f;
-          ls8[(j >> 1) & 7] += x0 + x1;
-          pk[j >> 1] = pack_f16x2(x0, x1);
-        }
-        tmem_st16(cs + c * 16, pk);
-      }
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      // pass 2: P = exp(s - m) as fp16 pairs, row sum of the fp32 values
+      const float lsum = full ? tile_row_exp<false>(cs, jmax, prm.c2, mxc)
+                              : tile_row_exp<true>(cs, jmax, prm.c2, mxc);
       if (it + 2 < my_n) {  // this warpgroup's next task
         const TaskView tn = decode_task(rec1);
         jmax_c = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
@@ -553,16 +602,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 10-13)
-    // Each thread owns one tile row: it stages its scaled 128-float row in
-    // shared memory (rows padded to 528 B so the lanes of a wavefront hit
-    // different banks) and adds it to the pool with one 512 B bulk reduction.
+    // Each thread owns one tile row.  A warp's 32 rows are the 16 heads of
+    // two queries; the warp stages them in the 128-byte-swizzled box layout of
+    // the pool's tensor map (conflict-free: the eight rows of a store phase
+    // hit eight different 16-byte bank groups) and one lane adds them to the
+    // pool with four bulk tensor reductions per query.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
     const int qi = row >> 4, hh = row & 15;
-    const uint32_t stage_row = sbase + kSmStage + uint32_t(row) * kStageRowBytes;
+    const uint32_t stage_q = sbase + kSmStage + uint32_t(qi) * 8192u;
+    const uint32_t stage_row = stage_q + uint32_t(hh) * 128u;
+    const uint32_t swz = uint32_t(hh & 7);
+    if (lane == 0 && my_n > 0) tma_prefetch_desc(&mapPool);
     int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
-    bool pending = false;
     // the row's token and the block's V scale are loaded one task ahead
     int32_t tok_c = my_n > 0 ? task_token(p.col, decode_task(rec), qi) : 0;
     float vmax_c = my_n > 0 ? prm.vmax[rec.w] : 0.f;
@@ -586,38 +639,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float alpha = s_alpha[st][row];
       const float lrow = s_lrow[st][row];
       const float mul = alpha / v_scale_in(vmx);
-      if (pending) bulk_wait_read0();  // this row's previous bulk reduction read the stage
-      uint32_t v[64];
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld32(tmem + lane_base + 256 + st * 128 + h * 64,
-                  *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tmem + lane_base + 256 + st * 128 + h * 64 + 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_ld_wait();
-        if (h == 1) {
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bars.o_free[st]));
-        }
+      // Boxes 0-1 (columns 0-63) and 2-3 (columns 64-127) of the warp's two
+      // queries go out as two bulk groups, so the bulk engine reads one pair
+      // while the warp stages the other: before a pair is overwritten, the
+      // previous task's group for it must have been read (wait_group.read 1
+      // leaves only the most recent group pending).
+      const uint32_t obase = tmem + lane_base + 256 + st * 128;
+      const int32_t tok_hi = __shfl_sync(0xffffffffu, tok, 16);
+      auto stage_box = [&](int cq, const uint32_t (&v)[32]) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          st_shared_v4(stage_row + h * 256 + u * 16,
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(stage_row + uint32_t(cq) * 2048u + ((uint32_t(u) ^ swz) << 4),
                        __float_as_uint(__uint_as_float(v[4 * u + 0]) * mul),
                        __float_as_uint(__uint_as_float(v[4 * u + 1]) * mul),
                        __float_as_uint(__uint_as_float(v[4 * u + 2]) * mul),
                        __float_as_uint(__uint_as_float(v[4 * u + 3]) * mul));
-      }
-      if (valid) {
-        fence_proxy_async_smem();
-        bulk_reduce_add_f32(prm.pool + grow * kHeadDim, stage_row, kHeadDim * 4);
+      };
+      auto issue_pair = [&](int cq0) {  // boxes cq0, cq0 + 1 of both queries
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int qj = 2 * quad + j;
+          if (qj < tv.nq) {
+            const int y = (j ? tok_hi : tok) * kQHeads + tv.g * kHeadsPerGroup;
+#pragma unroll
+            for (int cq = cq0; cq < cq0 + 2; ++cq)
+              tma_reduce_add_2d(&mapPool, sbase + kSmStage + uint32_t(qj) * 8192u + cq * 2048u,
+                                cq * 32, y);
+          }
+        }
         bulk_commit();
-        pending = true;
-        atomicAdd(prm.lsum + grow, alpha * lrow);
-      }
+      };
+      uint32_t v0[32], v1[32];
+      tmem_ld32(obase, v0);
+      tmem_ld32(obase + 32, v1);
+      if (lane == 0) bulk_wait_read1();  // previous task's boxes 0-1 read
+      __syncwarp();
+      tmem_ld_wait();
+      reg_fence32(v0);
+      reg_fence32(v1);
+      stage_box(0, v0);
+      stage_box(1, v1);
+      tmem_ld32(obase + 64, v0);
+      tmem_ld32(obase + 96, v1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue_pair(0);
+      __syncwarp();
+      tmem_ld_wait();
+      reg_fence32(v0);
+      reg_fence32(v1);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.o_free[st]));  // O_part read: the MMA may reuse the stage
+      if (lane == 0) bulk_wait_read1();  // previous task's boxes 2-3 read
+      __syncwarp();
+      stage_box(2, v0);
+      stage_box(3, v1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue_pair(2);
+      if (valid) atomicAdd(prm.lsum + grow, alpha * lrow);
       rec = rec1;
       rec1 = rec2;
     }
-    if (pending) bulk_wait0();  // bulk reductions complete before the CTA exits
+    if (lane == 0) bulk_wait0();  // bulk reductions complete before the CTA exits
   }
 
   // ---------------- teardown
@@ -748,6 +832,7 @@ __global__ void __launch_bounds__(256) k_fwd_fallback(msa_plan p, const __nv_bfl
 // ------------------------------------------------------------ host side
 CUresult make_map_rows(CUtensorMap* m, const void* base, int64_t rows);      // msa_api.cu
 CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T);           // msa_api.cu
+CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows);    // msa_api.cu
 int device_sm_count();                                                       // msa_api.cu
 
 size_t forward_workspace_bytes(const msa_plan& p) { return fwd_layout(p).total; }
@@ -764,9 +849,10 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   int32_t* list = reinterpret_cast<int32_t*>(w + L.off_list);
   const float c2 = scale * kLog2e;
 
-  CUtensorMap mQ, mK, mV;
+  CUtensorMap mQ, mK, mV, mPool;
   if (make_map_rows(&mQ, q, p.T * kQHeads) != CUDA_SUCCESS ||
-      make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS)
+      make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS ||
+      make_map_pool32(&mPool, pool, p.T * kQHeads) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   cudaError_t e;
@@ -789,7 +875,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   }
   FwdParams prm{p, M2, vmax, pool, lsum, c2, 16};
   launch_begin("fwd_main", s);
-  k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV);
+  k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
   launch_end("fwd_main", s);
   launch_begin("fwd_finalize", s);
   k_fwd_finalize<<<unsigned(device_sm_count() * 16), 256, 0, s>>>(

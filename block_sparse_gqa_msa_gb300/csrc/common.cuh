@@ -20,9 +20,6 @@ constexpr int kBlock = 128;         // keys per block
 constexpr int kTopK = 16;           // q2k slots
 constexpr int kTaskQueries = 8;     // queries per task: 8 x 16 heads = 128 rows
 constexpr int kMaxTokens = 1 << 20;
-// Rows (heads) per bulk tensor reduction into the 16-bit dQ pool: the tensor
-// map's box height (a divisor of the 16 heads of an index head).
-constexpr unsigned kDqReduceRows = 16;
 
 // Header slots (int64) in the plan workspace.
 enum HeaderSlot {

@@ -163,20 +163,19 @@ CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// [rows, 128] 16-bit pool (dQ accumulation) as the destination of bulk
-// tensor reductions; box = kDqReduceRows rows x 128 columns, no swizzle
-// (dense rows of 256 bytes).
-CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows, bool bf16) {
+// [rows, 128] fp32 pool (forward O accumulation) as the destination of bulk
+// tensor reductions; box = 16 rows x 32 columns (128 bytes), 128-byte swizzle,
+// so a tile row staged by one thread is spread over all shared-memory banks.
+CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows) {
   auto fn = encode_fn();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t gd[2] = {cuuint64_t(kHeadDim), cuuint64_t(rows)};
-  cuuint64_t gs[1] = {cuuint64_t(kHeadDim * 2)};
-  cuuint32_t box[2] = {128, kDqReduceRows};
+  cuuint64_t gs[1] = {cuuint64_t(kHeadDim * 4)};
+  cuuint32_t box[2] = {32, 16};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-            const_cast<void*>(base), gd, gs, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gd, gs, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 }  // namespace msa
