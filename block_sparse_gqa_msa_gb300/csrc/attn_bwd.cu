@@ -10,13 +10,14 @@
 //   dV  += P^T dO,  dK += dS^T Q   (A operands read from TMEM; cols 256, 384)
 //   dQ^T = K^T dS^T                 (dS from shared memory; cols [128,256))
 // TMEM lane = key for S/dP/dV/dK, so the per-key softmax work is one thread
-// per key; lane = head dimension for dQ^T, so a warp adds 32 consecutive head
-// dimensions of a pair of query heads at a time.  dV / dK accumulate over a
-// run of tasks that share the K/V block and are flushed with fp32 L2
-// reductions.  dQ goes straight from registers into a head-pair-interleaved
-// pool (the two heads of a pair side by side per head dimension) with packed
-// 16-bit atomics (fp16 by default, bf16 or fp32 on request): each warp-wide
-// atomic covers 128 contiguous bytes, and no shared memory is involved.
+// per key; lane = head dimension for dQ^T, so a thread holds one head
+// dimension of all the task's query heads.  dV / dK accumulate over a run of
+// tasks that share the K/V block and are flushed with fp32 L2 reductions.
+// dQ goes straight from registers into a pool interleaved by head octets
+// (the eight heads 8o..8o+7 of a token side by side per head dimension) with
+// 16-byte packed atomics (fp16 by default, bf16 or fp32 on request): a
+// warp-wide atomic covers 512 contiguous bytes, and no shared memory is
+// involved.
 //
 // bwd_main runs 14 warps: a TMA producer, an MMA issuer, eight compute warps
 // (P^T, dS^T, dQ^T readout; two per TMEM lane quadrant, each owning 64
@@ -603,25 +604,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence32(v1);
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dq_free));  // dP^T(it+1) may overwrite dQ^T(it)
-        // q-rows 16 k + 2 m, 16 k + 2 m + 1 are heads 2 m, 2 m + 1 of query
-        // 4 half + k: one pool word (two 16-bit or two fp32 values) per head
-        // dimension; lanes hold consecutive head dimensions.
+        // q-rows 16 k + 8 o .. 16 k + 8 o + 7 are the heads of octet o of
+        // query 4 half + k: one 16-byte atomic (two for fp32) per octet
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           if (4 * half + k >= tv0.nq) continue;
-          const int64_t pr0 = int64_t(tq[k]) * (kQHeads / 2) + tv0.g * (kHeadsPerGroup / 2);
+          const int64_t oct0 = int64_t(tq[k]) * (kQHeads / 8) + tv0.g * (kHeadsPerGroup / 8);
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const int j = 16 * k + 2 * m;
-            const float a = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]) * prm.scale;
-            const float b = __uint_as_float(j < 32 ? v0[j + 1] : v1[j - 31]) * prm.scale;
-            const int64_t e = ((pr0 + m) * kHeadDim + r) * 2;
-            if (ACC == MSA_DQ_ACCUM_F32)
-              red_add_v2_f32(static_cast<float*>(prm.dq_pool) + e, a, b);
-            else if (ACC == MSA_DQ_ACCUM_BF16)
-              red_add_bf16x2(static_cast<__nv_bfloat16*>(prm.dq_pool) + e, pack_bf16x2(a, b));
-            else
-              red_add_f16x2(static_cast<__half*>(prm.dq_pool) + e, pack_f16x2(a, b));
+          for (int o = 0; o < 2; ++o) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = 16 * k + 8 * o + e;
+              x[e] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]) * prm.scale;
+            }
+            const int64_t el = ((oct0 + o) * kHeadDim + r) * 8;
+            if (ACC == MSA_DQ_ACCUM_F32) {
+              float* dst = static_cast<float*>(prm.dq_pool) + el;
+              red_add_v4_f32(dst, x[0], x[1], x[2], x[3]);
+              red_add_v4_f32(dst + 4, x[4], x[5], x[6], x[7]);
+            } else if (ACC == MSA_DQ_ACCUM_BF16) {
+              red_add_v4_bf16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_bf16x2(x[0], x[1]),
+                                pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                                pack_bf16x2(x[6], x[7]));
+            } else {
+              red_add_v4_f16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_f16x2(x[0], x[1]),
+                               pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                               pack_f16x2(x[6], x[7]));
+            }
           }
         }
       }
@@ -682,54 +692,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------ bwd_finalize
-// Pools -> bf16 outputs.  dQ: one thread per (token, head pair, 8 head
-// dimensions) reads the 16 interleaved pool values and writes 8 dims of each
-// head; dK / dV: 8 elements per thread.
+// Pools -> bf16 outputs.  dQ: one thread per (head octet of a token, 8 head
+// dimensions) reads the 64 interleaved pool values and writes 8 dims of each
+// of the octet's heads; dK / dV: 8 elements per thread.
 __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq_pool,
                                                       const float* dk_pool, const float* dv_pool,
                                                       __nv_bfloat16* dq, __nv_bfloat16* dk,
                                                       __nv_bfloat16* dv) {
   if (plan_failed(p.header)) return;
-  const int64_t nq = p.T * (kQHeads / 2) * (kHeadDim / 8);
+  const int64_t nq = p.T * (kQHeads / 8) * (kHeadDim / 8);
   const int64_t nk8 = p.T * kKVHeads * kHeadDim / 8;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq + 2 * nk8;
        i += stride) {
     if (i < nq) {
-      const int64_t pr = i >> 4;  // token * 32 + head pair
+      const int64_t oct = i >> 4;  // token * 8 + head octet
       const int d0 = int(i & 15) * 8;
-      float f0[8], f1[8];  // heads 2 hp and 2 hp + 1
+      uint32_t out[8][4];  // [head in octet][dims pair]
       if (p.dq_accum == MSA_DQ_ACCUM_F32) {
         const float4* src = reinterpret_cast<const float4*>(
-            static_cast<const float*>(dq_pool) + (pr * kHeadDim + d0) * 2);
+            static_cast<const float*>(dq_pool) + (oct * kHeadDim + d0) * 8);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 a = src[u];
-          f0[2 * u] = a.x; f1[2 * u] = a.y; f0[2 * u + 1] = a.z; f1[2 * u + 1] = a.w;
+        for (int e = 0; e < 8; e += 2) {  // dims d0 + e, d0 + e + 1
+          const float4 a0 = src[2 * e], a1 = src[2 * e + 1];
+          const float4 b0 = src[2 * e + 2], b1 = src[2 * e + 3];
+          const float fa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const float fb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int h = 0; h < 8; ++h) out[h][e / 2] = pack_bf16x2(fa[h], fb[h]);
         }
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(dq_pool) + (pr * kHeadDim + d0) * 2);
-        const uint4 a = src[0], b = src[1];
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            static_cast<const uint16_t*>(dq_pool) + (oct * kHeadDim + d0) * 8);
+        const bool f16 = p.dq_accum == MSA_DQ_ACCUM_F16;
+        auto val = [&](uint32_t w, bool hi) {
+          return f16 ? (hi ? f16_hi(w) : f16_lo(w)) : (hi ? bf16_hi(w) : bf16_lo(w));
+        };
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (p.dq_accum == MSA_DQ_ACCUM_F16) {
-            f0[e] = f16_lo(w[e]);
-            f1[e] = f16_hi(w[e]);
-          } else {
-            f0[e] = bf16_lo(w[e]);
-            f1[e] = bf16_hi(w[e]);
-          }
+        for (int e = 0; e < 8; e += 2) {
+          const uint4 a = src[e], b = src[e + 1];
+          const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            out[h][e / 2] = pack_bf16x2(val(wa[h >> 1], h & 1), val(wb[h >> 1], h & 1));
         }
       }
-      __nv_bfloat16* o = dq + (2 * pr) * kHeadDim + d0;
-      *reinterpret_cast<uint4*>(o) =
-          make_uint4(pack_bf16x2(f0[0], f0[1]), pack_bf16x2(f0[2], f0[3]),
-                     pack_bf16x2(f0[4], f0[5]), pack_bf16x2(f0[6], f0[7]));
-      *reinterpret_cast<uint4*>(o + kHeadDim) =
-          make_uint4(pack_bf16x2(f1[0], f1[1]), pack_bf16x2(f1[2], f1[3]),
-                     pack_bf16x2(f1[4], f1[5]), pack_bf16x2(f1[6], f1[7]));
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        *reinterpret_cast<uint4*>(dq + (oct * 8 + h) * kHeadDim + d0) =
+            make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
     } else {
       const int64_t j = i < nq + nk8 ? i - nq : i - nq - nk8;
       const float* src = i < nq + nk8 ? dk_pool : dv_pool;

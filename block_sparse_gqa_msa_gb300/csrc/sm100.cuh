@@ -439,6 +439,19 @@ __device__ __forceinline__ void red_add_f32(float* gptr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(v) : "memory");
 }
 
+// 16-byte packed reductions: four 16-bit pairs (eight values) per thread.
+__device__ __forceinline__ void red_add_v4_f16x2(void* gptr, uint32_t a, uint32_t b, uint32_t c,
+                                                 uint32_t d) {
+  asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red_add_v4_bf16x2(void* gptr, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d) {
+  asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
 __device__ __forceinline__ void red_add_v2_f32(float* gptr, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(gptr), "f"(a), "f"(b) : "memory");
 }
