@@ -139,14 +139,17 @@ struct BwdParams {
   float* dv_pool;
   float c2;     // scale * log2(e)
   float scale;
-  int chunk;
   int dq_accum;
 };
 
-__device__ __forceinline__ int64_t cta_task(int64_t i, int chunk) {
-  return (int64_t(blockIdx.x) + (i / chunk) * gridDim.x) * chunk + (i % chunk);
+// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
+// index arithmetic runs on the MMA issuer's critical path).
+constexpr int kBwdChunk = 64;
+__device__ __forceinline__ int64_t cta_task(int64_t i) {
+  return (int64_t(blockIdx.x) + (i / kBwdChunk) * gridDim.x) * kBwdChunk + (i % kBwdChunk);
 }
-__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
+__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
+  constexpr int chunk = kBwdChunk;
   const int64_t nchunks = (ntasks + chunk - 1) / chunk;
   if (int64_t(blockIdx.x) >= nchunks) return 0;
   const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;
@@ -154,9 +157,12 @@ __device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
   return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
                                                                     : chunk);
 }
-// Task record i of this CTA's walk, or an empty record past the end.
-__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n, int chunk) {
-  return i < n ? tasks[cta_task(i, chunk)] : make_int4(0, 0, 1 << 8, -1);
+// Task record i of this CTA's walk; past the end, the last one (every
+// caller guards its uses by the index).  Only the address depends on the
+// index test, never the loaded value, so nothing waits for the load until
+// the record is used.  With no tasks, entry 0 of the (allocated) table.
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
+  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
 }
 __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
@@ -175,7 +181,7 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
 // soon as P^T(t) is in TMEM, and the compute warps read dQ^T(t) out while
 // S^T(t+1) runs.
 __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t sbase,
-                                          const int4* tasks, int64_t my_n, int chunk,
+                                          const int4* tasks, int64_t my_n,
                                           volatile int* abort_flag) {
   constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
   constexpr uint32_t idKM = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
@@ -233,8 +239,8 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   };
   int64_t kv_loads = 1, seg_done = 0;
   bool first_in_seg = true;
-  int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
-  int next_kv = task_rec(tasks, 1, my_n, chunk).w;
+  int cur_kv = task_rec(tasks, 0, my_n).w;
+  int next_kv = task_rec(tasks, 1, my_n).w;
   bool ok = wait(bars.kv_full, 0) && wait(bars.qdo_full[0], 0);
   if (ok) {
     issue_S(0);
@@ -242,7 +248,7 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   }
   for (int64_t it = 0; ok && it < my_n; ++it) {
     const uint32_t ph = uint32_t(it & 1);
-    const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;  // used next iteration
+    const int next2_kv = task_rec(tasks, it + 2, my_n).w;  // used next iteration
     const uint32_t acc0 = first_in_seg ? 0u : 1u;
     // the first dV / dK of a run overwrite the accumulators: the reducers
     // must have flushed the previous run
@@ -350,9 +356,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
-  const int64_t my_n = cta_task_count(ntasks, prm.chunk);
+  const int64_t my_n = cta_task_count(ntasks);
   const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
-  const int chunk = prm.chunk;
 
   if (warp == 0) {
     // ---------------- TMA producer (task records and tokens prefetched one task ahead)
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
-      int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+      int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
       int32_t tok[kTaskQueries];
       {
         const TaskView tv = decode_task(rec);
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       for (; it < my_n; ++it) {
         const TaskView tv = decode_task(rec);
-        const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+        const int4 rec2 = task_rec(tasks, it + 2, my_n);
         int32_t tok1[kTaskQueries];
         {
           const TaskView tv1 = decode_task(rec1);
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, my_n, chunk, abort_flag);
+    if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, my_n, abort_flag);
   } else if (warp < 10) {
     // ---------------- compute (thread = TMEM lane; half = block of 64 q-rows)
     // Phase 1 (after S^T; thread = key): P = 2^(S^T c2 - LSE log2 e), masked
@@ -456,14 +461,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool wf = __all_sync(0xffffffffu, jl == kBlock - 1);
       if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
     };
-    int4 rec0 = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    int4 rec0 = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
     int32_t tok1 = 0;
-    if (half == 0 && my_n > 0) {
-      const TaskView tv = decode_task(rec0);
-      const int32_t tok = task_token(p.col, tv, qi);
-      const int64_t grow = col_row(tv, tok);
-      put_cols(prm.lse[grow], prm.delta[grow], col_jlim(tv, tok));
-      if (my_n > 1) tok1 = task_token(p.col, decode_task(rec1), qi);
+    if (my_n > 0) {
+      tok1 = task_token(p.col, decode_task(rec1), qi);
+      if (half == 0) {
+        const TaskView tv = decode_task(rec0);
+        const int32_t tok = task_token(p.col, tv, qi);
+        const int64_t grow = col_row(tv, tok);
+        put_cols(prm.lse[grow], prm.delta[grow], col_jlim(tv, tok));
+      }
     }
     // Column scalars of a task are published through the `cols` barrier
     // (phase 0: task 0; phase it + 1: task it + 1).  Half 0 overwrites them
@@ -497,17 +504,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int64_t it = 0; cols_ok && it < my_n; ++it) {
       const uint32_t ph = uint32_t(it & 1);
       const int st = int(it & 1);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
-      // the next task's column scalars: issued now, stored after phase 2
-      float lse1 = 0.f, dl1 = 0.f;
-      int jl1 = -1;
-      if (half == 0 && it + 1 < my_n) {
-        const TaskView tv1 = decode_task(rec1);
-        const int64_t grow = col_row(tv1, tok1);
-        lse1 = prm.lse[grow];
-        dl1 = prm.delta[grow];
-        jl1 = col_jlim(tv1, tok1);
-      }
+      const int4 rec2 = task_rec(tasks, it + 2, my_n);
+      // The next task's column scalars: loaded now (unconditionally, so no
+      // select waits for them here), stored by half 0 after phase 2.
+      const TaskView tv1 = decode_task(rec1);
+      const int64_t grow1 = col_row(tv1, tok1);
+      const float lse1 = prm.lse[grow1];
+      const float dl1 = prm.delta[grow1];
+      const int jl1 = col_jlim(tv1, tok1);
       const bool full = (s_wfull[0] & s_wfull[1] & s_wfull[2] & s_wfull[3]) != 0;
       const float* nl = &s_nlse2[half * 64];
       const float* dlt = &s_delta[half * 64];
@@ -531,8 +535,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_ready[half]));
-      int32_t tok2 = 0;
-      if (half == 0 && it + 2 < my_n) tok2 = task_token(p.col, decode_task(rec2), qi);
+      const int32_t tok2 = task_token(p.col, decode_task(rec2), qi);
       // tokens of the half's four queries, for the dQ atomics of phase 3
       const TaskView tv0 = decode_task(rec0);
       int32_t tq[4];
@@ -644,11 +647,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quad = warp & 3;
     const int key = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
     int64_t nseg = 0;
     for (int64_t it = 0; it < my_n; ++it) {
       const TaskView tv = decode_task(rec);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      const int4 rec2 = task_rec(tasks, it + 2, my_n);
       const bool seg_end = (it + 1 == my_n) || rec1.w != tv.sub;
       if (seg_end) {
         // seg_done follows the run's last dV / dK MMAs: the accumulators are final
@@ -797,8 +800,7 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
     }
     attr_set = true;
   }
-  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, 64,
-                p.dq_accum};
+  BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, p.dq_accum};
   launch_begin("bwd_main", s);
   const unsigned grid = unsigned(device_sm_count());
   if (p.dq_accum == MSA_DQ_ACCUM_F32)

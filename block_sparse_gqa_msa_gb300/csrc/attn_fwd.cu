@@ -227,15 +227,18 @@ struct FwdParams {
   float* pool;
   float* lsum;
   float c2;
-  int chunk;
 };
 
-// Task i of the CTA's walk: chunks of `chunk` consecutive tasks go round-robin
+// Task i of the CTA's walk: chunks of kFwdChunk consecutive tasks go round-robin
 // over the CTAs, so all CTAs advance through the task list together.
-__device__ __forceinline__ int64_t cta_task(int64_t i, int chunk) {
-  return (int64_t(blockIdx.x) + (i / chunk) * gridDim.x) * chunk + (i % chunk);
+// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
+// index arithmetic runs on the MMA issuer's critical path).
+constexpr int kFwdChunk = 16;
+__device__ __forceinline__ int64_t cta_task(int64_t i) {
+  return (int64_t(blockIdx.x) + (i / kFwdChunk) * gridDim.x) * kFwdChunk + (i % kFwdChunk);
 }
-__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
+__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
+  constexpr int chunk = kFwdChunk;
   const int64_t nchunks = (ntasks + chunk - 1) / chunk;
   if (int64_t(blockIdx.x) >= nchunks) return 0;
   const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;  // chunks of this CTA
@@ -243,8 +246,12 @@ __device__ __forceinline__ int64_t cta_task_count(int64_t ntasks, int chunk) {
   return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
                                                                     : chunk);
 }
-__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n, int chunk) {
-  return i < n ? tasks[cta_task(i, chunk)] : make_int4(0, 0, 1 << 8, -1);
+// Task record i of this CTA's walk; past the end, the last one (every
+// caller guards its uses by the index).  Only the address depends on the
+// index test, never the loaded value, so nothing waits for the load until
+// the record is used.  With no tasks, entry 0 of the (allocated) table.
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
+  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
 }
 __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
@@ -340,7 +347,7 @@ __device__ __forceinline__ float tile_row_exp(uint32_t cs, int jmax, float c2, f
 // MMA issuer of k_fwd_main (one thread).  A function of its own so its few
 // live values stay in registers whatever the other roles need.
 __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t sbase,
-                                          const int4* tasks, int64_t my_n, int chunk,
+                                          const int4* tasks, int64_t my_n,
                                           volatile int* abort_flag) {
   constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T   (bf16)
   constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, P in TMEM)
@@ -378,12 +385,12 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
     need_v = true;
     return true;
   };
-  int cur_kv = task_rec(tasks, 0, my_n, chunk).w;
-  int next_kv = task_rec(tasks, 1, my_n, chunk).w;
+  int cur_kv = task_rec(tasks, 0, my_n).w;
+  int next_kv = task_rec(tasks, 1, my_n).w;
   ok = wait_kv() && issue_S(0);
   for (int64_t it = 0; ok && it < my_n; ++it) {
     const int st = int(it & 1);
-    const int next2_kv = task_rec(tasks, it + 2, my_n, chunk).w;
+    const int next2_kv = task_rec(tasks, it + 2, my_n).w;
     const bool same = (it + 1 < my_n) && next_kv == cur_kv;
     if (same && !issue_S(it + 1)) break;
     if (!wait(bars.p_full[st], uint32_t((it >> 1) & 1))) break;
@@ -451,9 +458,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
-  const int64_t my_n = cta_task_count(ntasks, prm.chunk);
+  const int64_t my_n = cta_task_count(ntasks);
   const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
-  const int chunk = prm.chunk;
 
   if (warp == 0) {
     // ---------------- TMA producer (records and tokens prefetched one task ahead)
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
-      int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+      int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
       int32_t tok[kTaskQueries];
       {
         const TaskView tv = decode_task(rec);
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       for (; it < my_n; ++it) {
         const TaskView tv = decode_task(rec);
-        const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+        const int4 rec2 = task_rec(tasks, it + 2, my_n);
         int32_t tok1[kTaskQueries];
         {
           const TaskView tv1 = decode_task(rec1);
@@ -519,14 +525,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, my_n, chunk, abort_flag);
+    if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, my_n, abort_flag);
   } else if (warp == 14) {
     // ---------------- V tile bf16 -> fp16 (scaled by an exact power of two)
     if (my_n > 0) {
       int prev_kv = -1;
       int64_t kv_loads = 0;
       for (int64_t it = 0; it < my_n; ++it) {
-        const int kv = task_rec(tasks, it, my_n, chunk).w;
+        const int kv = task_rec(tasks, it, my_n).w;
         if (kv == prev_kv) continue;
         prev_kv = kv;
         const float sc = v_scale_in(prm.vmax[kv]);
@@ -556,11 +562,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // runs, in two steps so no load result is consumed right after it is
     // issued: the row's token at the top of task it, its shift M after the
     // exponentials.
-    int4 rec1 = task_rec(tasks, par + 2, my_n, chunk);
+    int4 rec1 = task_rec(tasks, par + 2, my_n);
     int jmax_c = -1;
     float m2_c = 0.f;
     if (par < my_n) {
-      const TaskView tv = decode_task(task_rec(tasks, par, my_n, chunk));
+      const TaskView tv = decode_task(task_rec(tasks, par, my_n));
       const int32_t tok = task_token(p.col, tv, qi);
       jmax_c = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
       m2_c = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
@@ -569,8 +575,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int st = int(it & 1);
       const int jmax = jmax_c;
       const float m2 = m2_c;
-      const int4 rec2 = task_rec(tasks, it + 4, my_n, chunk);
-      const int32_t ntok = it + 2 < my_n ? task_token(p.col, decode_task(rec1), qi) : 0;
+      const int4 rec2 = task_rec(tasks, it + 4, my_n);
+      // (loads of the next task's row data are unconditional - rec1 is a
+      // valid record even past the end - so nothing waits for them here)
+      const int32_t ntok = task_token(p.col, decode_task(rec1), qi);
       if (!mbar_wait_warp(smem_u32(&bars.s_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       tc_fence_after();
       const uint32_t cs = tmem + lane_base + st * 128;
@@ -583,7 +591,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // pass 2: P = exp(s - m) as fp16 pairs, row sum of the fp32 values
       const float lsum = full ? tile_row_exp<false>(cs, jmax, prm.c2, mxc)
                               : tile_row_exp<true>(cs, jmax, prm.c2, mxc);
-      if (it + 2 < my_n) {  // this warpgroup's next task
+      {  // this warpgroup's next task
         const TaskView tn = decode_task(rec1);
         jmax_c = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
         m2_c = prm.M2[int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh];
@@ -615,20 +623,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t stage_row = stage_q + uint32_t(hh) * 128u;
     const uint32_t swz = uint32_t(hh & 7);
     if (lane == 0 && my_n > 0) tma_prefetch_desc(&mapPool);
-    int4 rec = task_rec(tasks, 0, my_n, chunk), rec1 = task_rec(tasks, 1, my_n, chunk);
+    int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
     // the row's token and the block's V scale are loaded one task ahead
     int32_t tok_c = my_n > 0 ? task_token(p.col, decode_task(rec), qi) : 0;
     float vmax_c = my_n > 0 ? prm.vmax[rec.w] : 0.f;
     for (int64_t it = 0; it < my_n; ++it) {
       const int st = int(it & 1);
       const TaskView tv = decode_task(rec);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n, chunk);
+      const int4 rec2 = task_rec(tasks, it + 2, my_n);
       const int32_t tok = tok_c;
       const float vmx = vmax_c;
-      if (it + 1 < my_n) {
-        tok_c = task_token(p.col, decode_task(rec1), qi);
-        vmax_c = prm.vmax[rec1.w];
-      }
+      tok_c = task_token(p.col, decode_task(rec1), qi);  // rec1: a valid record
+      vmax_c = prm.vmax[rec1.w];
       const bool valid = qi < tv.nq;
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
       if (!mbar_wait_warp(smem_u32(&bars.o_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
@@ -873,7 +879,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  FwdParams prm{p, M2, vmax, pool, lsum, c2, 16};
+  FwdParams prm{p, M2, vmax, pool, lsum, c2};
   launch_begin("fwd_main", s);
   k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
   launch_end("fwd_main", s);
