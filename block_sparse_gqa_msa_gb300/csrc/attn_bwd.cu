@@ -17,7 +17,10 @@
 // (the eight heads 8o..8o+7 of a token side by side per head dimension) with
 // 16-byte packed atomics (fp16 by default, bf16 or fp32 on request): a
 // warp-wide atomic covers 512 contiguous bytes, and no shared memory is
-// involved.
+// involved.  A warp issues such atomics only one every ~200 cycles, so the
+// twelve warps that can reach a TMEM lane quadrant share them: the eight
+// compute warps take the first 32 q-rows of their half, the four flush warps
+// the other 32 of each half.
 //
 // bwd_main runs 14 warps: a TMA producer, an MMA issuer, eight compute warps
 // (P^T, dS^T, dQ^T readout; two per TMEM lane quadrant, each owning 64
@@ -295,13 +298,49 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   mbar_wait_drain(smem_u32(&bars.fin), 0);
 }
 
+// Adds dQ^T of two queries (q0, q0+1 of the task; 32 q-rows = 4 head octets,
+// values v of head dimension d) to the octet-interleaved pool: one 16-byte
+// packed atomic per octet (two for fp32).
+template <int ACC>
+__device__ __forceinline__ void dq_atomics(const BwdParams& prm, const uint32_t (&v)[32],
+                                           const int32_t (&tok)[2], const TaskView& tv, int q0,
+                                           int d) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (q0 + k >= tv.nq) continue;
+    const int64_t oct0 = int64_t(tok[k]) * (kQHeads / 8) + tv.g * (kHeadsPerGroup / 8);
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[16 * k + 8 * o + e]) * prm.scale;
+      const int64_t el = ((oct0 + o) * kHeadDim + d) * 8;
+      if (ACC == MSA_DQ_ACCUM_F32) {
+        float* dst = static_cast<float*>(prm.dq_pool) + el;
+        red_add_v4_f32(dst, x[0], x[1], x[2], x[3]);
+        red_add_v4_f32(dst + 4, x[4], x[5], x[6], x[7]);
+      } else if (ACC == MSA_DQ_ACCUM_BF16) {
+        red_add_v4_bf16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_bf16x2(x[0], x[1]),
+                          pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                          pack_bf16x2(x[6], x[7]));
+      } else {
+        red_add_v4_f16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_f16x2(x[0], x[1]),
+                         pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                         pack_f16x2(x[6], x[7]));
+      }
+    }
+  }
+}
+
 // Warp roles (448 threads):
 //   0      TMA producer: K/V per block run, Q/dO per task (two stages)
 //   1      MMA issuer, TMEM owner
-//   2-9    compute: P^T, dS^T (TMEM) and dS (shared memory), then dQ^T read
-//          out of TMEM and added to the pool with packed atomics; warps 2-5
-//          own q-rows [0,64), warps 6-9 [64,128)
-//   10-13  dV / dK flush at the end of a run (thread = key)
+//   2-9    compute: P^T, dS^T (TMEM) and dS (shared memory), then dQ^T of
+//          q-rows [64h, 64h+32) read out of TMEM and added to the pool with
+//          packed atomics; warps 2-5 own q-rows [0,64) (h = 0), warps 6-9
+//          [64,128) (h = 1)
+//   10-13  dQ^T of q-rows [32,64) and [96,128) (thread = head dim); dV / dK
+//          flush at the end of a run (thread = key)
 template <int ACC>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_main(const __grid_constant__ BwdParams prm, const __grid_constant__ CUtensorMap mapQ,
@@ -340,7 +379,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&bars.pt_free), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
-    mbar_init(smem_u32(&bars.dq_free), 256);
+    mbar_init(smem_u32(&bars.dq_free), 384);
     mbar_init(smem_u32(&bars.seg_done), 1);
     mbar_init(smem_u32(&bars.dkv_free), 128);
     mbar_init(smem_u32(&bars.cols), 256);
@@ -434,8 +473,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (A operand of dV) and kept in registers.  Phase 2 (after dP^T):
     // dS = P (dP^T - delta) as bf16 into TMEM (A operand of dK) and into the
     // shared-memory dS tile (row = key, 128-byte swizzle; B operand of dQ^T).
-    // Phase 3 (after dQ^T; thread = head dim): dQ^T read out, scaled and
-    // added to the head-pair-interleaved pool with packed atomics.
+    // Phase 3 (after dQ^T; thread = head dim): dQ^T of q-rows [64h, 64h+32)
+    // (queries 4h, 4h+1) read out, scaled and added to the pool with packed
+    // atomics.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // key (phases 1, 2) / head dim (phase 3) = TMEM lane
@@ -536,11 +576,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_ready[half]));
       const int32_t tok2 = task_token(p.col, decode_task(rec2), qi);
-      // tokens of the half's four queries, for the dQ atomics of phase 3
+      // tokens of the queries 4h, 4h+1, for the dQ atomics of phase 3
       const TaskView tv0 = decode_task(rec0);
-      int32_t tq[4];
+      int32_t tq[2];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tq[k] = task_token(p.col, tv0, 4 * half + k);
+      for (int k = 0; k < 2; ++k) tq[k] = task_token(p.col, tv0, 4 * half + k);
       // ---- phase 2
       if (!mbar_wait_warp(smem_u32(&bars.dp_full), ph, abort_flag)) break;
       tc_fence_after();
@@ -599,51 +639,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // every MMA of the task is complete: its Q / dO stage is free
       if (warp == 2 && lane == 0) mbar_arrive(smem_u32(&bars.qdo_empty[st]));
       {
-        uint32_t v0[32], v1[32];
+        uint32_t v0[32];
         tmem_ld32(cQ, v0);
-        tmem_ld32(cQ + 32, v1);
         tmem_ld_wait();
         reg_fence32(v0);
-        reg_fence32(v1);
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dq_free));  // dP^T(it+1) may overwrite dQ^T(it)
-        // q-rows 16 k + 8 o .. 16 k + 8 o + 7 are the heads of octet o of
-        // query 4 half + k: one 16-byte atomic (two for fp32) per octet
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (4 * half + k >= tv0.nq) continue;
-          const int64_t oct0 = int64_t(tq[k]) * (kQHeads / 8) + tv0.g * (kHeadsPerGroup / 8);
-#pragma unroll
-          for (int o = 0; o < 2; ++o) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int j = 16 * k + 8 * o + e;
-              x[e] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]) * prm.scale;
-            }
-            const int64_t el = ((oct0 + o) * kHeadDim + r) * 8;
-            if (ACC == MSA_DQ_ACCUM_F32) {
-              float* dst = static_cast<float*>(prm.dq_pool) + el;
-              red_add_v4_f32(dst, x[0], x[1], x[2], x[3]);
-              red_add_v4_f32(dst + 4, x[4], x[5], x[6], x[7]);
-            } else if (ACC == MSA_DQ_ACCUM_BF16) {
-              red_add_v4_bf16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_bf16x2(x[0], x[1]),
-                                pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                                pack_bf16x2(x[6], x[7]));
-            } else {
-              red_add_v4_f16x2(static_cast<uint16_t*>(prm.dq_pool) + el, pack_f16x2(x[0], x[1]),
-                               pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                               pack_f16x2(x[6], x[7]));
-            }
-          }
-        }
+        dq_atomics<ACC>(prm, v0, tq, tv0, 4 * half, r);
       }
       rec0 = rec1;
       rec1 = rec2;
       tok1 = tok2;
     }
   } else {
-    // ---------------- dV / dK flush at the end of each run (thread = key)
+    // ---------------- dQ^T of q-rows [32,64) and [96,128) (thread = head
+    // dim), dV / dK flush at the end of each run (thread = key)
     const int quad = warp & 3;
     const int key = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
@@ -652,6 +662,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int64_t it = 0; it < my_n; ++it) {
       const TaskView tv = decode_task(rec);
       const int4 rec2 = task_rec(tasks, it + 2, my_n);
+      int32_t ta[2], tb[2];  // tokens of queries 2, 3 and 6, 7
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        ta[k] = task_token(p.col, tv, 2 + k);
+        tb[k] = task_token(p.col, tv, 6 + k);
+      }
+      if (!mbar_wait_warp(smem_u32(&bars.dq_full), uint32_t(it & 1), abort_flag)) break;
+      tc_fence_after();
+      {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tmem + lane_base + kTmDQ + 32, va);
+        tmem_ld32(tmem + lane_base + kTmDQ + 96, vb);
+        tmem_ld_wait();
+        reg_fence32(va);
+        reg_fence32(vb);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_free));
+        dq_atomics<ACC>(prm, va, ta, tv, 2, key);
+        dq_atomics<ACC>(prm, vb, tb, tv, 6, key);
+      }
       const bool seg_end = (it + 1 == my_n) || rec1.w != tv.sub;
       if (seg_end) {
         // seg_done follows the run's last dV / dK MMAs: the accumulators are final

@@ -198,15 +198,15 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
 //   0     TMA producer: K/V per block run, Q per task (two stages)
 //   1     MMA issuer (TMEM owner): S = Q K^T, O_part = P V with P read from TMEM
 //   2-9   softmax (thread = tile row = TMEM lane): row max, P = exp(s - m) as
-//         fp16 written over the row's S columns, row sum; warps 2-5 take the
-//         even tasks (TMEM stage 0), warps 6-9 the odd ones (stage 1)
+//         fp16 into the stage's P columns, row sum; warps 2-5 take the even
+//         tasks (TMEM stage 0), warps 6-9 the odd ones (stage 1)
 //   10-13 epilogue (thread = tile row): O_part * exp(m - M) staged in shared
 //         memory and added to the fp32 pool by bulk tensor reductions (four
 //         2 KB boxes per query, issued by one lane per warp); row sums by
 //         atomics
 //   14    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
-// TMEM: S (and P over its first 64 columns) in [0,128) / [128,256), O_part in
-// [256,384) / [384,512), two stages each.
+// TMEM: S in two stages, P (fp16) of each stage in columns of its own, one
+// O_part stage (see kTmP0, kTmO).
 constexpr int kFwdThreads = 480;
 constexpr uint32_t kTileBytes = 32768;
 constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
@@ -215,9 +215,15 @@ constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
 constexpr uint32_t kStageBytes = kTaskQueries * 8192;
 constexpr uint32_t kFwdSmem = kSmStage + kStageBytes + 1024;
 
+// TMEM columns: S in two stages [0,128) and [128,256); P of stage st (fp16
+// pairs) in [256 + 64 st, 320 + 64 st); one O_part stage [384,512).  P has
+// columns of its own so that S(t+2) can overwrite S(t) as soon as the
+// softmax has read it, without waiting for P(t).V.
+constexpr uint32_t kTmP0 = 256, kTmO = 384;
+
 struct FwdBars {
-  uint64_t kv_full, kv_empty, v_ready, q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2],
-      o_free[2], fin;
+  uint64_t kv_full, kv_empty, v_ready, q_full[2], q_empty[2], s_full[2], s_free[2], p_full[2],
+      pv_done[2], rs_free[2], o_full, o_free, fin;
 };
 
 struct FwdParams {
@@ -303,7 +309,8 @@ __device__ __forceinline__ float tile_row_max(uint32_t cs, int jmax) {
 // the next 16 columns are loaded while the current ones are exponentiated.
 // Returns the row sum of the fp32 values.
 template <bool MASK>
-__device__ __forceinline__ float tile_row_exp(uint32_t cs, int jmax, float c2, float mxc) {
+__device__ __forceinline__ float tile_row_exp(uint32_t cs, uint32_t cp, int jmax, float c2,
+                                             float mxc) {
   const uint64_t cc = f2_pack(__float_as_uint(c2), __float_as_uint(c2));
   const uint64_t nm = f2_pack(__float_as_uint(-mxc), __float_as_uint(-mxc));
   uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
@@ -330,11 +337,11 @@ __device__ __forceinline__ float tile_row_exp(uint32_t cs, int jmax, float c2, f
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     tmem_ld16(cs + 32 * i + 16, r1);
-    expo(r0, jmax - 32 * i, cs + 16 * i);
+    expo(r0, jmax - 32 * i, cp + 16 * i);
     tmem_ld_wait();
     reg_fence16(r1);
     if (i < 3) tmem_ld16(cs + 32 * i + 32, r0);
-    expo(r1, jmax - 32 * i - 16, cs + 16 * i + 8);
+    expo(r1, jmax - 32 * i - 16, cp + 16 * i + 8);
     if (i < 3) {
       tmem_ld_wait();
       reg_fence16(r0);
@@ -365,11 +372,11 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
   auto mstep = [](int kk) { return uint64_t(kk) * 128u; };
   int64_t kv_loads = 0;
   bool ok = true, need_v = false;
-  // S(it) goes to stage it&1, whose P(it-2) must have been read by PV(it-2).
+  // S(it) goes to stage it&1, which the softmax of task it-2 must have read.
   auto issue_S = [&](int64_t it) -> bool {
     const int st = int(it & 1);
     if (!wait(bars.q_full[st], uint32_t((it >> 1) & 1))) return false;
-    if (it >= 2 && !wait(bars.o_full[st], uint32_t(((it >> 1) - 1) & 1))) return false;
+    if (it >= 2 && !wait(bars.s_free[st], uint32_t(((it >> 1) - 1) & 1))) return false;
     tc_fence_after();
     const uint64_t bq = kQ0 + uint64_t(st) * kStage;
 #pragma unroll
@@ -394,7 +401,8 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
     const bool same = (it + 1 < my_n) && next_kv == cur_kv;
     if (same && !issue_S(it + 1)) break;
     if (!wait(bars.p_full[st], uint32_t((it >> 1) & 1))) break;
-    if (it >= 2 && !wait(bars.o_free[st], uint32_t(((it >> 1) - 1) & 1))) break;
+    // one O_part stage: the epilogue must have read O_part(it-1)
+    if (it >= 1 && !wait(bars.o_free, uint32_t((it - 1) & 1))) break;
     if (need_v) {
       if (!wait(bars.v_ready, uint32_t((kv_loads - 1) & 1))) break;
       need_v = false;
@@ -402,8 +410,9 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      umma_ts(tmem + 256 + st * 128, tmem + st * 128 + kk * 8, mV + mstep(kk), idPV, kk > 0);
-    umma_commit(smem_u32(&bars.o_full[st]));
+      umma_ts(tmem + kTmO, tmem + kTmP0 + st * 64 + kk * 8, mV + mstep(kk), idPV, kk > 0);
+    umma_commit(smem_u32(&bars.o_full));
+    umma_commit(smem_u32(&bars.pv_done[st]));
     if (it + 1 < my_n && !same) {
       umma_commit(smem_u32(&bars.kv_empty));
       cur_kv = next_kv;
@@ -442,10 +451,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&bars.q_full[i]), 1);
       mbar_init(smem_u32(&bars.q_empty[i]), 1);
       mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.s_free[i]), 128);
       mbar_init(smem_u32(&bars.p_full[i]), 128);
-      mbar_init(smem_u32(&bars.o_full[i]), 1);
-      mbar_init(smem_u32(&bars.o_free[i]), 128);
+      mbar_init(smem_u32(&bars.pv_done[i]), 1);
+      mbar_init(smem_u32(&bars.rs_free[i]), 128);
     }
+    mbar_init(smem_u32(&bars.o_full), 1);
+    mbar_init(smem_u32(&bars.o_free), 128);
     mbar_init(smem_u32(&bars.fin), 1);
     fence_mbar_init();
   }
@@ -588,18 +600,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // pass 1: the tile row's maximum over visible keys (raw scores)
       const float mx = full ? tile_row_max<false>(cs, jmax) : tile_row_max<true>(cs, jmax);
       const float mxc = (jmax >= 0) ? mx * prm.c2 : 0.f;
-      // pass 2: P = exp(s - m) as fp16 pairs, row sum of the fp32 values
-      const float lsum = full ? tile_row_exp<false>(cs, jmax, prm.c2, mxc)
-                              : tile_row_exp<true>(cs, jmax, prm.c2, mxc);
+      // pass 2: P = exp(s - m) as fp16 pairs into this stage's P columns
+      // (P.V of task it-2 must have read them), row sum of the fp32 values
+      if (it >= 2 &&
+          !mbar_wait_warp(smem_u32(&bars.pv_done[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
+        break;
+      const uint32_t cp = tmem + lane_base + kTmP0 + st * 64;
+      const float lsum = full ? tile_row_exp<false>(cs, cp, jmax, prm.c2, mxc)
+                              : tile_row_exp<true>(cs, cp, jmax, prm.c2, mxc);
+      // S(it) is fully read: S(it+2) may overwrite the stage
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.s_free[st]));
       {  // this warpgroup's next task
         const TaskView tn = decode_task(rec1);
         jmax_c = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
         m2_c = prm.M2[int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh];
       }
-      // the epilogue of task it-2 has read this stage's row scalars once it
-      // released O_part (o_free)
+      // the epilogue of task it-2 has read this stage's row scalars
       if (it >= 2 &&
-          !mbar_wait_warp(smem_u32(&bars.o_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
+          !mbar_wait_warp(smem_u32(&bars.rs_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
         break;
       s_alpha[st][row] = jmax >= 0 ? fast_exp2(mxc - m2) : 0.f;
       s_lrow[st][row] = lsum;
@@ -637,20 +656,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       vmax_c = prm.vmax[rec1.w];
       const bool valid = qi < tv.nq;
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
-      if (!mbar_wait_warp(smem_u32(&bars.o_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
+      if (!mbar_wait_warp(smem_u32(&bars.o_full), uint32_t(it & 1), abort_flag)) break;
       // p_full(it) completed before o_full(it); waiting on it makes the
       // softmax's row scalars visible here.
       if (!mbar_wait_warp(smem_u32(&bars.p_full[st]), uint32_t((it >> 1) & 1), abort_flag)) break;
       tc_fence_after();
       const float alpha = s_alpha[st][row];
       const float lrow = s_lrow[st][row];
+      mbar_arrive(smem_u32(&bars.rs_free[st]));
       const float mul = alpha / v_scale_in(vmx);
       // Boxes 0-1 (columns 0-63) and 2-3 (columns 64-127) of the warp's two
       // queries go out as two bulk groups, so the bulk engine reads one pair
       // while the warp stages the other: before a pair is overwritten, the
       // previous task's group for it must have been read (wait_group.read 1
       // leaves only the most recent group pending).
-      const uint32_t obase = tmem + lane_base + 256 + st * 128;
+      const uint32_t obase = tmem + lane_base + kTmO;
       const int32_t tok_hi = __shfl_sync(0xffffffffu, tok, 16);
       auto stage_box = [&](int cq, const uint32_t (&v)[32]) {
 #pragma unroll
@@ -695,7 +715,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       reg_fence32(v0);
       reg_fence32(v1);
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.o_free[st]));  // O_part read: the MMA may reuse the stage
+      mbar_arrive(smem_u32(&bars.o_free));  // O_part read: the next P.V may overwrite it
       if (lane == 0) bulk_wait_read1();  // previous task's boxes 2-3 read
       __syncwarp();
       stage_box(2, v0);
