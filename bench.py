@@ -494,12 +494,15 @@ def run_gpu(args, rank, world):
 
 
 def main():
+    global WORKLOAD
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--super-block", type=int, default=64)
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5],
+                    help="synthetic workload (default: the packed 16k row the metric is quoted on)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-adjacent", action="store_true",
@@ -509,6 +512,7 @@ def main():
     ap.add_argument("--sample-max-tokens", type=int, default=0,
                     help="reference arm: cut sampled documents to this prefix (0 = whole)")
     args = ap.parse_args()
+    WORKLOAD = args.workload
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -11,10 +11,12 @@
 // without a second pass over the scores.  Each task exponentiates against its
 // own tile row maximum m (P = exp(s - m) in (0, 1], fp16 for the P.V product)
 // and rescales its partial P.V and row sum by exp(m - M) onto a per-row shift
-// M[t,h] = scale * |q_th| * max_{selected v} max_{j in v} |k_jg| shared by all
-// tasks of the row; M bounds every score of the row (Cauchy-Schwarz), so the
-// rescaled partials add up in fp32 pools with L2 bulk reductions.  The
-// finalize divides.  Rows whose sum underflows (the bound far above the true
+// M[t,h] shared by all tasks of the row: the Cauchy-Schwarz bound
+// scale * |q_th| * max_{selected v} max_{j in v} |k_jg| on every score of the
+// row, lowered by a fixed headroom so that a loose bound (a few keys of large
+// norm) does not push the sum towards underflow.  The rescaled partials add up
+// in fp32 pools with L2 bulk reductions; the finalize divides.  Rows whose sum
+// still underflows (the bound more than headroom + 60 octaves above the true
 // maximum) are recomputed exactly by a fallback kernel.
 //
 // Kernels, in launch order:
@@ -143,11 +145,21 @@ __global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat1
 }
 
 // ------------------------------------------------------------ fwd_rows
-// One warp per (token, index head): M2 = c2 * |q_th| * kmax_sel for the 16
-// heads (-inf when the row sees no key), and zero the row's pool and sum.
+// One warp per (token, index head): the shift M2 of each of the 16 heads'
+// rows (-inf when the row sees no key), and zero the row's pool and sum.
+//
+// The Cauchy-Schwarz bound B = c2 * |q_th| * kmax_sel (log2 units) is never
+// below the row's true maximum m, but may sit far above it (a few keys of
+// large norm).  The shift is placed H below it, M2 = B - H, so that the row's
+// pooled sum 2^(m - M2) * (...) underflows only when B - m > H + 60.  A
+// partial is then scaled by at most 2^H, so the pool holds at most
+// 2^H * 2^11 * vmax_sel (2048 keys, P <= 1): H = 64, lowered for rows whose
+// selected blocks hold |v| above 2^48, keeps that below 2^124.
+constexpr float kShiftHeadroom = 64.f;
 __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat16* Q,
-                                                  const float* kmax, float c2, float* M2,
-                                                  float* lsum, float* pool) {
+                                                  const float* kmax, const float* vmax,
+                                                  float c2, float* M2, float* lsum,
+                                                  float* pool) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
@@ -156,13 +168,23 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
   const int d = doc_of_token(p.doc_offsets, p.num_docs, t);
   const DocInfo di = reinterpret_cast<const DocInfo*>(p.doc_info)[d];
   const int64_t qb = (t - di.start) / kBlock;
-  float km = -1.f;
+  float km = -1.f, vm = 0.f;
   if (lane < kTopK) {
     const int32_t v = p.q2k[(int64_t(g) * p.T + t) * kTopK + lane];
-    if (v >= 0 && v <= qb) km = kmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+    if (v >= 0 && v <= qb) {
+      km = kmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+      vm = vmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  }
+  // vm may be inf or nan (non-finite V): no headroom then.
+  const float headroom =
+      (vm <= 281474976710656.f) ? kShiftHeadroom
+                                : (vm < INFINITY ? fmaxf(0.f, 112.f - ceilf(log2f(vm))) : 0.f);
   // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
   const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
   float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
@@ -183,7 +205,7 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
     for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (sub == 0) {
       const int64_t row = t * kQHeads + g * kHeadsPerGroup + hh;
-      M2[row] = km < 0.f ? -INFINITY : c2 * sqrtf(s) * km;
+      M2[row] = km < 0.f ? -INFINITY : c2 * sqrtf(s) * km - headroom;
       lsum[row] = 0.f;
     }
   }
@@ -890,7 +912,7 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
   k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, c2, M2, lsum, pool);
+      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
   launch_end("fwd_rows", s);
 
   static bool attr_set = false;
