@@ -393,7 +393,7 @@ def run_gpu(args, rank, world):
     h_out = (ho, hlse, hdq, hdk, hdv)
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = sum(x.numel() * x.element_size() for x in h_out)
-    e2e_steps = max(4, args.steps // 2)
+    e2e_steps = max(4, args.steps)  # as many steps as the device-timed loop
     e2e_ms = float("nan")
     if not args.no_e2e:
         sets_in = [tuple(torch.empty_like(x, device=dev) for x in h_in) for _ in range(2)]
