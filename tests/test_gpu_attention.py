@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from block_sparse_gqa_msa_gb300 import api, inputs
-from tests.helpers import check_grad, check_lse, check_o
+from tests.helpers import check_grad, check_lse, check_o, rel_fro
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -139,3 +139,41 @@ def test_repeat_calls_reuse_plan():
         o, lse = api.msa_forward(plan, q, k, v, w.scale)
     check_o(o.float().cpu().numpy(), O)
     check_lse(lse.cpu().numpy(), L)
+
+
+def _golden(name):
+    """key -> float from a "key value" fixture under tests/golden/."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    out = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                out[line[0]] = float(line[1])
+    return out
+
+
+def test_error_level_within_pages_range():
+    # The pages' own kernels land at 1.9e-3 to 2.9e-3 relative L2 error on
+    # O / dQ / dK / dV at T = 4k..16k, one document, top-16, fp16 dQ pool
+    # (tests/golden/pages_accuracy.txt), measured against a second bf16
+    # implementation.  Same setting here, measured against the exact (fp64)
+    # result: every output must show an error of the same size, at most 1.5x
+    # their worst figure (measured here: O 1.6e-3, dV 2.3e-3, dK and dQ
+    # 3.0e-3; dQ and dK carry the rounding of dS to bf16 for the tensor-core
+    # products, which the sums' cancellation amplifies).  O at T = 4k; the
+    # gradients on the one-document 2125-token case (the fp64 oracle's
+    # backward at 4k takes minutes; the per-element error level does not
+    # depend on T).
+    g = _golden("pages_accuracy.txt")
+    w = inputs.custom([int(g["t_low"])], 41)
+    O, _ = oracle.Problem.from_workload(w).forward()
+    o, *_ = run_gpu(w, super_block=64, dq_accum="f16")
+    errs = {"O": rel_fro(o, O)}
+    w2, _, _, dQ, dK, dV = oracle_results("uniform-2k")
+    _, _, dq, dk, dv = run_gpu(w2, super_block=64, dq_accum="f16")
+    errs.update(dQ=rel_fro(dq, dQ), dK=rel_fro(dk, dK), dV=rel_fro(dv, dV))
+    print("relative L2 error vs fp64:", {n: f"{e:.2e}" for n, e in errs.items()})
+    for n, e in errs.items():
+        assert e <= 1.5 * g["rel_l2_high"], f"{n}: relative L2 error {e:.3e}"
