@@ -314,7 +314,7 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
     q, k, v, do = (x.to(dev) for x in (w.q, w.k, w.v, w.do))
     q2k, offs = w.q2k.to(dev), w.doc_offsets.to(dev)
-    plan = api.msa_build_plan(q2k, offs, super_block=args.super_block)
+    plan = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum)
     pws = plan.workspace
     fws = torch.empty(api.forward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     bws = torch.empty(api.backward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
@@ -324,7 +324,8 @@ def run_gpu(args, rank, world):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
-        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, workspace=pws)
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum,
+                                 workspace=pws)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
         api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
         return p
@@ -355,7 +356,8 @@ def run_gpu(args, rank, world):
         flush.zero_()
         e = evs[i]
         e[0].record(stream)
-        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, workspace=pws)
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum,
+                                 workspace=pws)
         e[1].record(stream)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
         e[2].record(stream)
@@ -420,7 +422,8 @@ def run_gpu(args, rank, world):
                 stream.wait_event(out_done[b])
             qq, kk, vv, dd, q2, of = sets_in[b]
             oo, ll = sets_out[b][0], sets_out[b][1]
-            pp = api.msa_build_plan(q2, of, super_block=args.super_block, workspace=pws)
+            pp = api.msa_build_plan(q2, of, super_block=args.super_block, o_accum=args.o_accum,
+                                 workspace=pws)
             api.msa_forward(pp, qq, kk, vv, w.scale, o=oo, lse=ll, workspace=fws)
             api.msa_backward(pp, qq, kk, vv, oo, ll, dd, w.scale, dq=dq_, dk=dk_, dv=dv_,
                              workspace=bws)
@@ -467,7 +470,7 @@ def run_gpu(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "T": T, "docs": w.num_docs, "heads": "64q/4kv/4idx",
-                   "head_dim": 128, "block": 128, "topk": 16, "super_block": args.super_block,
+                   "head_dim": 128, "block": 128, "topk": 16, "super_block": args.super_block, "o_pool": args.o_accum,
                    "pairs": pairs, "flop_per_step": flop_step,
                    "l2": "flushed before each timed step (256 MiB write)"},
         "tokens_per_s": tok_s,
@@ -501,6 +504,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--super-block", type=int, default=64)
+    ap.add_argument("--o-accum", choices=["f32", "bf16"], default="f32",
+                    help="precision of the forward's O pool")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5],
                     help="synthetic workload (default: the packed 16k row the metric is quoted on)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -37,6 +37,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kUnderflowSum = 8.673617379884035e-19f;
 
 // ------------------------------------------------------------ workspace
+// Bytes per element of the O pool (fp32, or bf16 on request).
+inline size_t pool_elem_bytes(const msa_plan& p) { return p.o_accum == MSA_O_ACCUM_BF16 ? 2 : 4; }
+
 struct FwdLayout {
   size_t off_m, off_l, off_pool, off_kmax, off_vmax, off_list, total;
 };
@@ -46,7 +49,7 @@ FwdLayout fwd_layout(const msa_plan& p) {
   size_t o = 0;
   L.off_m = o;    o = align_up(o + sizeof(float) * rows, 256);
   L.off_l = o;    o = align_up(o + sizeof(float) * rows, 256);
-  L.off_pool = o; o = align_up(o + sizeof(float) * rows * kHeadDim, 256);
+  L.off_pool = o; o = align_up(o + pool_elem_bytes(p) * rows * kHeadDim, 256);
   L.off_kmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
   L.off_vmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
   L.off_list = o; o = align_up(o + sizeof(int32_t) * (rows + 1), 256);
@@ -159,7 +162,7 @@ constexpr float kShiftHeadroom = 64.f;
 __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat16* Q,
                                                   const float* kmax, const float* vmax,
                                                   float c2, float* M2, float* lsum,
-                                                  float* pool) {
+                                                  uint8_t* pool, int pool_esz) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
                                 : (vm < INFINITY ? fmaxf(0.f, 112.f - ceilf(log2f(vm))) : 0.f);
   // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
   const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-  float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
+  uint8_t* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim * pool_esz;
   const int half = lane >> 4, sub = lane & 15;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
@@ -209,10 +212,11 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
       lsum[row] = 0.f;
     }
   }
-  float4* z = reinterpret_cast<float4*>(prow);
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint4* z = reinterpret_cast<uint4*>(prow);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const int n16 = kHeadsPerGroup * kHeadDim * pool_esz / 16;
 #pragma unroll 4
-  for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
+  for (int i = lane; i < n16; i += 32) z[i] = zero;
 }
 
 // ------------------------------------------------------------ fwd_main
@@ -252,7 +256,7 @@ struct FwdParams {
   msa_plan plan;
   const float* M2;
   const float* vmax;
-  float* pool;
+  void* pool;
   float* lsum;
   float c2;
 };
@@ -447,6 +451,9 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
   mbar_wait_drain(smem_u32(&bars.fin), 0);
 }
 
+// POOL_BF16: the O pool is bf16 (boxes of 64 columns) instead of fp32 (boxes
+// of 32 columns).
+template <bool POOL_BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_main(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -655,7 +662,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // two queries; the warp stages them in the 128-byte-swizzled box layout of
     // the pool's tensor map (conflict-free: the eight rows of a store phase
     // hit eight different 16-byte bank groups) and one lane adds them to the
-    // pool with four bulk tensor reductions per query.
+    // pool with four (fp32 pool) or two (bf16 pool) bulk tensor reductions
+    // per query.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
@@ -717,6 +725,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         bulk_commit();
       };
+      // bf16 pool: box b holds columns [64b, 64b + 64) of the 16 rows; chunk u
+      // of a row (columns 64b + 8u ...) comes from a (u < 4) or b (u >= 4).
+      auto stage_box16 = [&](int b, const uint32_t (&a)[32], const uint32_t (&c)[32]) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t (&v)[32] = u < 4 ? a : c;
+          const int k = (u & 3) * 8;
+          st_shared_v4(stage_row + uint32_t(b) * 2048u + ((uint32_t(u) ^ swz) << 4),
+                       pack_bf16x2(__uint_as_float(v[k + 0]) * mul, __uint_as_float(v[k + 1]) * mul),
+                       pack_bf16x2(__uint_as_float(v[k + 2]) * mul, __uint_as_float(v[k + 3]) * mul),
+                       pack_bf16x2(__uint_as_float(v[k + 4]) * mul, __uint_as_float(v[k + 5]) * mul),
+                       pack_bf16x2(__uint_as_float(v[k + 6]) * mul, __uint_as_float(v[k + 7]) * mul));
+        }
+      };
+      auto issue_box16 = [&](int b) {  // box b of both queries
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int qj = 2 * quad + j;
+          if (qj < tv.nq) {
+            const int y = (j ? tok_hi : tok) * kQHeads + tv.g * kHeadsPerGroup;
+            tma_reduce_add_2d(&mapPool, sbase + kSmStage + uint32_t(qj) * 8192u + b * 2048u,
+                              b * 64, y);
+          }
+        }
+        bulk_commit();
+      };
       uint32_t v0[32], v1[32];
       tmem_ld32(obase, v0);
       tmem_ld32(obase + 32, v1);
@@ -725,13 +759,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld_wait();
       reg_fence32(v0);
       reg_fence32(v1);
-      stage_box(0, v0);
-      stage_box(1, v1);
+      if constexpr (POOL_BF16) {
+        stage_box16(0, v0, v1);
+      } else {
+        stage_box(0, v0);
+        stage_box(1, v1);
+      }
       tmem_ld32(obase + 64, v0);
       tmem_ld32(obase + 96, v1);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) issue_pair(0);
+      if (lane == 0) {
+        if constexpr (POOL_BF16)
+          issue_box16(0);
+        else
+          issue_pair(0);
+      }
       __syncwarp();
       tmem_ld_wait();
       reg_fence32(v0);
@@ -740,11 +783,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive(smem_u32(&bars.o_free));  // O_part read: the next P.V may overwrite it
       if (lane == 0) bulk_wait_read1();  // previous task's boxes 2-3 read
       __syncwarp();
-      stage_box(2, v0);
-      stage_box(3, v1);
+      if constexpr (POOL_BF16) {
+        stage_box16(1, v0, v1);
+      } else {
+        stage_box(2, v0);
+        stage_box(3, v1);
+      }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) issue_pair(2);
+      if (lane == 0) {
+        if constexpr (POOL_BF16)
+          issue_box16(1);
+        else
+          issue_pair(2);
+      }
       if (valid) atomicAdd(prm.lsum + grow, alpha * lrow);
       rec = rec1;
       rec1 = rec2;
@@ -764,8 +816,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // eight rows per step (16 lanes x 8 elements per row), all loads issued
 // before any use.  Rows whose sum underflowed are listed for the fallback.
 constexpr int kFinRowsPerWarp = 8;
+template <bool POOL_BF16>
 __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M2,
-                                                      const float* lsum, const float* pool,
+                                                      const float* lsum, const void* pool,
                                                       __nv_bfloat16* O, float* lse,
                                                       int32_t* list) {
   if (plan_failed(p.header)) return;
@@ -775,14 +828,22 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
   for (int64_t r0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32 * kFinRowsPerWarp;
        r0 < rows; r0 += nwarps * kFinRowsPerWarp) {
     float4 a[4], b[4];
+    uint4 h[4];  // bf16 pool: the 8 elements, widened after all loads
     float m2[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t row = r0 + 2 * i + (lane >> 4);
       if (row < rows) {
-        const float4* src = reinterpret_cast<const float4*>(pool + row * kHeadDim) + 2 * sub;
-        a[i] = src[0];
-        b[i] = src[1];
+        if constexpr (POOL_BF16) {
+          h[i] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(pool) +
+                                                row * kHeadDim)[sub];
+        } else {
+          const float4* src =
+              reinterpret_cast<const float4*>(static_cast<const float*>(pool) + row * kHeadDim) +
+              2 * sub;
+          a[i] = src[0];
+          b[i] = src[1];
+        }
         m2[i] = M2[row];
         l[i] = lsum[row];
       } else {
@@ -805,6 +866,10 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
           continue;  // the fallback kernel writes this row
         }
         const float inv = 1.f / l[i];
+        if constexpr (POOL_BF16) {
+          a[i] = make_float4(bf16_lo(h[i].x), bf16_hi(h[i].x), bf16_lo(h[i].y), bf16_hi(h[i].y));
+          b[i] = make_float4(bf16_lo(h[i].z), bf16_hi(h[i].z), bf16_lo(h[i].w), bf16_hi(h[i].w));
+        }
         out = make_uint4(pack_bf16x2(a[i].x * inv, a[i].y * inv), pack_bf16x2(a[i].z * inv, a[i].w * inv),
                          pack_bf16x2(b[i].x * inv, b[i].y * inv), pack_bf16x2(b[i].z * inv, b[i].w * inv));
         L = (m2[i] + __log2f(l[i])) * kLn2;
@@ -881,6 +946,7 @@ __global__ void __launch_bounds__(256) k_fwd_fallback(msa_plan p, const __nv_bfl
 CUresult make_map_rows(CUtensorMap* m, const void* base, int64_t rows);      // msa_api.cu
 CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T);           // msa_api.cu
 CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows);    // msa_api.cu
+CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows);    // msa_api.cu
 int device_sm_count();                                                       // msa_api.cu
 
 size_t forward_workspace_bytes(const msa_plan& p) { return fwd_layout(p).total; }
@@ -892,7 +958,8 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   float* M2 = reinterpret_cast<float*>(w + L.off_m);
   float* lsum = reinterpret_cast<float*>(w + L.off_l);
   float* vmax = reinterpret_cast<float*>(w + L.off_vmax);
-  float* pool = reinterpret_cast<float*>(w + L.off_pool);
+  uint8_t* pool = w + L.off_pool;
+  const bool pool16 = p.o_accum == MSA_O_ACCUM_BF16;
   float* kmax = reinterpret_cast<float*>(w + L.off_kmax);
   int32_t* list = reinterpret_cast<int32_t*>(w + L.off_list);
   const float c2 = scale * kLog2e;
@@ -900,7 +967,8 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   CUtensorMap mQ, mK, mV, mPool;
   if (make_map_rows(&mQ, q, p.T * kQHeads) != CUDA_SUCCESS ||
       make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS ||
-      make_map_pool32(&mPool, pool, p.T * kQHeads) != CUDA_SUCCESS)
+      (pool16 ? make_map_pool16(&mPool, pool, p.T * kQHeads)
+              : make_map_pool32(&mPool, pool, p.T * kQHeads)) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   cudaError_t e;
@@ -912,22 +980,32 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
   k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
+      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool,
+      int(pool_elem_bytes(p)));
   launch_end("fwd_rows", s);
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(k_fwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[pool16]) {
+    e = cudaFuncSetAttribute(pool16 ? k_fwd_main<true> : k_fwd_main<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[pool16] = true;
   }
   FwdParams prm{p, M2, vmax, pool, lsum, c2};
+  const unsigned grid = unsigned(device_sm_count());
   launch_begin("fwd_main", s);
-  k_fwd_main<<<unsigned(device_sm_count()), kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
+  if (pool16)
+    k_fwd_main<true><<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
+  else
+    k_fwd_main<false><<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
   launch_end("fwd_main", s);
   launch_begin("fwd_finalize", s);
-  k_fwd_finalize<<<unsigned(device_sm_count() * 16), 256, 0, s>>>(
-      p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o), lse, list);
+  if (pool16)
+    k_fwd_finalize<true><<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool,
+                                                   static_cast<__nv_bfloat16*>(o), lse, list);
+  else
+    k_fwd_finalize<false><<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool,
+                                                    static_cast<__nv_bfloat16*>(o), lse, list);
   launch_end("fwd_finalize", s);
   launch_begin("fwd_fallback", s);
   k_fwd_fallback<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(

@@ -178,6 +178,20 @@ CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// The same pool in bf16: box = 16 rows x 64 columns (128 bytes), 128-byte
+// swizzle.
+CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t gd[2] = {cuuint64_t(kHeadDim), cuuint64_t(rows)};
+  cuuint64_t gs[1] = {cuuint64_t(kHeadDim * 2)};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -214,7 +228,9 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   if (T < 1 || T > kMaxTokens || num_docs < 1 || num_docs > T) return MSA_ERR_INVALID_ARG;
   const int32_t Z = opts ? opts->super_block : 64;
   const int32_t acc = opts ? opts->dq_accum : MSA_DQ_ACCUM_F16;
+  const int32_t oacc = opts ? opts->o_accum : MSA_O_ACCUM_F32;
   if (Z < 0 || acc < MSA_DQ_ACCUM_F16 || acc > MSA_DQ_ACCUM_F32) return MSA_ERR_INVALID_ARG;
+  if (oacc != MSA_O_ACCUM_F32 && oacc != MSA_O_ACCUM_BF16) return MSA_ERR_INVALID_ARG;
   if (!aligned16(q2k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(doc_offsets) & 3u))
     return MSA_ERR_ALIGNMENT;
   const PlanLayout L = plan_layout(T, num_docs);
@@ -227,6 +243,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   p.num_docs = num_docs;
   p.super_block = Z;
   p.dq_accum = acc;
+  p.o_accum = oacc;
   p.nb_cap = L.nb_cap;
   p.tri_cap = L.tri_cap;
   p.nnz_cap = L.nnz_cap;

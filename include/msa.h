@@ -78,6 +78,16 @@ typedef enum msa_dq_accum {
   MSA_DQ_ACCUM_F32 = 2
 } msa_dq_accum;
 
+/* Precision of the forward's O accumulation pool.  The up-to-16 block
+ * partials of an output row are added in a pool at a shared row shift; FP32
+ * keeps O's rounding to that of the final bf16 store, BF16 (same exponent
+ * range) halves the pool's shared-memory staging, L2 reduction and HBM
+ * traffic at the cost of an 8-bit mantissa in every addition. */
+typedef enum msa_o_accum {
+  MSA_O_ACCUM_F32 = 0,
+  MSA_O_ACCUM_BF16 = 1
+} msa_o_accum;
+
 /* Plan-build options.  Pass NULL for the defaults. */
 typedef struct msa_plan_options {
   /* Tasks of one (index head, key block) bucket are cut at runs of
@@ -85,7 +95,9 @@ typedef struct msa_plan_options {
   int32_t super_block;
   /* An msa_dq_accum value.  Default MSA_DQ_ACCUM_F16. */
   int32_t dq_accum;
-  int32_t reserved[6];
+  /* An msa_o_accum value.  Default (0) MSA_O_ACCUM_F32. */
+  int32_t o_accum;
+  int32_t reserved[5];
 } msa_plan_options;
 
 /*
@@ -108,7 +120,7 @@ typedef struct msa_plan {
   int32_t num_docs;
   int32_t super_block;
   int32_t dq_accum;
-  int32_t reserved0;
+  int32_t o_accum;
   int64_t nb_cap;     /* bound on the number of 128-key blocks            */
   int64_t tri_cap;    /* bound on (index head, doc, key block, query block) */
   int64_t nnz_cap;    /* bound on CSR entries                              */

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from block_sparse_gqa_msa_gb300 import api, inputs
-from tests.helpers import check_grad, check_lse, check_o, rel_fro
+from tests.helpers import O_POOL16_MAX_ABS, check_grad, check_lse, check_o, rel_fro
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -56,10 +56,10 @@ def oracle_results(name):
     return w, O, L, dQ, dK, dV
 
 
-def run_gpu(w, super_block=16, dq_accum="f16"):
+def run_gpu(w, super_block=16, dq_accum="f16", o_accum="f32"):
     q, k, v, do = (x.to(DEV) for x in (w.q, w.k, w.v, w.do))
     plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=super_block,
-                              dq_accum=dq_accum)
+                              dq_accum=dq_accum, o_accum=o_accum)
     o, lse = api.msa_forward(plan, q, k, v, w.scale)
     dq, dk, dv = api.msa_backward(plan, q, k, v, o, lse, do, w.scale)
     torch.cuda.synchronize()
@@ -73,6 +73,20 @@ def test_forward_matches_oracle(name):
     o, lse, *_ = run_gpu(w)
     check_o(o, O)
     check_lse(lse, L)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_bf16_pool_matches_oracle(name):
+    # O partials added in a bf16 pool (msa_plan_options.o_accum, opt-in): the
+    # same bar except O's max-abs error, which the pool's extra bf16 rounding
+    # can take to one bf16 ulp (O_POOL16_MAX_ABS).
+    w, O, L, dQ, dK, dV = oracle_results(name)
+    o, lse, dq, dk, dv = run_gpu(w, o_accum="bf16")
+    check_o(o, O, max_abs=O_POOL16_MAX_ABS)
+    check_lse(lse, L)
+    check_grad(dq, dQ, "dQ")
+    check_grad(dk, dK, "dK")
+    check_grad(dv, dV, "dV")
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -170,7 +184,8 @@ def test_error_level_within_pages_range():
     w = inputs.custom([int(g["t_low"])], 41)
     O, _ = oracle.Problem.from_workload(w).forward()
     o, *_ = run_gpu(w, super_block=64, dq_accum="f16")
-    errs = {"O": rel_fro(o, O)}
+    o16, *_ = run_gpu(w, super_block=64, dq_accum="f16", o_accum="bf16")
+    errs = {"O": rel_fro(o, O), "O (bf16 pool)": rel_fro(o16, O)}
     w2, _, _, dQ, dK, dV = oracle_results("uniform-2k")
     _, _, dq, dk, dv = run_gpu(w2, super_block=64, dq_accum="f16")
     errs.update(dQ=rel_fro(dq, dQ), dK=rel_fro(dk, dK), dV=rel_fro(dv, dV))
