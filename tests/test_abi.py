@@ -1,8 +1,13 @@
 """The C ABI without a GPU: libmsa.so builds and loads, exports every function
-include/msa.h declares, and rejects bad arguments on the host before any
+include/msa.h declares, the Python binding's structure mirrors match the
+header's layout, and bad arguments are rejected on the host before any
 launch."""
 import ctypes
+import os
 import re
+import shutil
+import subprocess
+import tempfile
 
 import pytest
 
@@ -116,3 +121,37 @@ def test_select_workspace_host_checks(lib):
     assert lib.msa_select_blocks(g, g, 100, 64, g, 1, 1, g, g, 16, None) == 4   # workspace
     assert lib.msa_select_blocks(ctypes.c_void_p(0x10008), g, 100, 64, g, 1, 1, g, g, 1 << 20,
                                  None) == 3                                     # alignment
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a C compiler")
+def test_struct_layouts_match_header():
+    # A C probe compiled against include/msa.h prints each structure's size,
+    # every field offset the binding declares, and the accumulator enums.
+    mirrors = {"msa_plan": api.MsaPlanStruct, "msa_plan_options": api.MsaPlanOptions}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "msa.h"', "int main(void) {"]
+    for cname, py in mirrors.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'  printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    for name in ("MSA_DQ_ACCUM_F16", "MSA_DQ_ACCUM_BF16", "MSA_DQ_ACCUM_F32",
+                 "MSA_O_ACCUM_F32", "MSA_O_ACCUM_BF16"):
+        lines.append(f'  printf("enum {name} %d\\n", (int){name});')
+    lines += ["  return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "probe.c"), os.path.join(d, "probe")
+        with open(src, "w") as f:
+            f.write("\n".join(lines) + "\n")
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(api.HEADER_PATH), src, "-o", exe],
+                       check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for line in out.splitlines():
+        a, b, v = line.split()
+        got[(a, b)] = int(v)
+    for cname, py in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert got[(cname, field)] == getattr(py, field).offset, (cname, field)
+    assert {k: got[("enum", "MSA_DQ_ACCUM_" + k.upper())] for k in api.DQ_ACCUM} == api.DQ_ACCUM
+    assert {k: got[("enum", "MSA_O_ACCUM_" + k.upper())] for k in api.O_ACCUM} == api.O_ACCUM
+
