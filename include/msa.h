@@ -181,7 +181,8 @@ msa_status msa_build_plan_static(const int32_t* q2k, const int32_t* doc_offsets,
                                  int32_t num_docs, const msa_plan_options* opts,
                                  msa_stream_t stream, msa_plan* out);
 
-/* Bytes of forward workspace for a plan (host only). */
+/* Bytes of forward workspace for a plan (host only).  Dominated by the O
+ * pool, T x 64 x 128 elements of the plan's o_accum type (4 or 2 bytes). */
 msa_status msa_forward_workspace_bytes(const msa_plan* plan, size_t* bytes);
 
 /*
