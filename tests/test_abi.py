@@ -63,9 +63,12 @@ def test_build_plan_host_checks(lib):
     # sizes
     assert lib.msa_build_plan(good, good, 0, 2, None, good, ws_n.value, None,
                               ctypes.byref(st)) == 1
-    bad_opts = api.MsaPlanOptions(super_block=-1)
-    assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(bad_opts), good, ws_n.value, None,
-                              ctypes.byref(st)) == 1
+    for bad_opts in (api.MsaPlanOptions(super_block=-1),
+                     api.MsaPlanOptions(super_block=16, dq_accum=3),
+                     api.MsaPlanOptions(super_block=16, o_accum=2),
+                     api.MsaPlanOptions(super_block=16, o_accum=-1)):
+        assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(bad_opts), good, ws_n.value,
+                                  None, ctypes.byref(st)) == 1
     # alignment
     assert lib.msa_build_plan(ctypes.c_void_p(0x10004), good, 1000, 2, ctypes.byref(opts), good,
                               ws_n.value, None, ctypes.byref(st)) == 3
