@@ -79,3 +79,25 @@ def test_reference_arm_under_torchrun():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_recorded_traffic_follows_the_sources(tmp_path, monkeypatch):
+    # The DRAM bytes of a committed ncu record count only while the kernel's
+    # sources hash to the value recorded with them.
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    rec = {"kernel": "k", "workload": "w", "bytes_per_launch": 123,
+           "source_files": ["k.cu"],
+           "source_sha256_16": hashlib.sha256(b"kernel v1\n").hexdigest()[:16]}
+    (tmp_path / "profiles" / "k_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k", "w") == 123
+    assert bench.recorded_traffic("k", "another workload") is None
+    assert bench.recorded_traffic("missing", "w") is None
+    src.write_text("kernel v2\n")
+    assert bench.recorded_traffic("k", "w") is None
+
