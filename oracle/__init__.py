@@ -89,6 +89,8 @@ def _bind(lib):
     lib.oracle_pair_count.restype = _I64
     lib.oracle_select_blocks.argtypes = [_P, _P, _I64, _I32, _P, _I32, _I32, _P]
     lib.oracle_select_blocks.restype = ctypes.c_int
+    lib.oracle_block_scores.argtypes = [_P, _P, _I64, _I32, _P, _I32, _P, _I64, _I64, _P]
+    lib.oracle_block_scores.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     for f in ("oracle_forward", "oracle_dq", "oracle_dkv_blocks", "oracle_backward",
@@ -259,8 +261,9 @@ def threads() -> int:
 
 
 def select_blocks(iq, ik, doc_offsets, force_local: bool = True) -> np.ndarray:
-    """q2k int32 [4, T, 16] chosen by the block scorer (see oracle_select_blocks
-    in msa_oracle.c).  iq, ik: bf16 [T, 4, dim] tensors or uint16 bit arrays."""
+    """q2k int32 [4, T, 16] chosen by the block scorer in fp64 (see
+    oracle_select_blocks in msa_oracle.c).  iq, ik: bf16 [T, 4, dim] tensors or
+    uint16 bit arrays."""
     a = _bf16_bits(iq)
     b = _bf16_bits(ik)
     if a.shape != b.shape or a.ndim != 3 or a.shape[1] != 4:
@@ -272,3 +275,21 @@ def select_blocks(iq, ik, doc_offsets, force_local: bool = True) -> np.ndarray:
                                       1 if force_local else 0, _ptr(q2k))
     _check(rc, "select_blocks")
     return q2k
+
+
+def block_scores(iq, ik, doc_offsets, rows) -> np.ndarray:
+    """fp64 scores of the candidate blocks 0..b of each listed (index head,
+    token) row: array [n, maxb], NaN past the row's own block b."""
+    a = _bf16_bits(iq)
+    b = _bf16_bits(ik)
+    if a.shape != b.shape or a.ndim != 3 or a.shape[1] != 4:
+        raise ValueError("iq and ik must both be [T, 4, dim]")
+    T, _, dim = a.shape
+    offs = _i32(doc_offsets)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+    maxb = int(np.diff(offs).max() + 127) // 128
+    out = np.zeros((rows.shape[0], maxb), dtype=np.float64)
+    rc = _load().oracle_block_scores(_ptr(a), _ptr(b), T, dim, _ptr(offs), offs.size - 1,
+                                     _ptr(rows), rows.shape[0], maxb, _ptr(out))
+    _check(rc, "block_scores")
+    return out

@@ -17,7 +17,7 @@
  *         queries times the 16 query heads of an index head, grouped by index
  *         head and key block; the delta preprocess), run_backward parameter list (LSE is FP32 [T,64]).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - query head h uses KV head and index head h/16;
  *   - key block v of a document covers document positions 128v..128v+127 (the
  *     last block may be partial);
@@ -521,8 +521,7 @@ int oracle_threads(void) {
  * Block selection: the index scorer and top-k that produce q2k.
  *
  * The pages name the step (an indexer scores the key blocks, each query
- * keeps the top 16) but print no scoring formula; the plainest reading, used
- * here and in the kernel:
+ * keeps the top 16) but print no scoring formula; the plainest reading:
  *   summary(g, d, v)[c] = mean over the keys j of document block v of
  *                         ik[j, g, c]   (block v = document positions
  *                         128v .. 128v+127, the last one may be partial)
@@ -533,22 +532,48 @@ int oracle_threads(void) {
  * sink block 0 and the query's own block b are always kept and 14 are chosen
  * among 1 .. b-1.  Slots hold the chosen blocks in ascending order, then -1.
  *
- * A ranking is decided by floating point, so this takes the decisions in the
- * kernel's precision and order of operations: fp32, the block sum
- * accumulated key by key (acc += x) and divided by the key count, the score
- * accumulated channel by channel with fused multiply-adds.
+ * Everything is fp64 on the exactly widened bf16 inputs.  A kernel that ranks
+ * in a lower precision can differ from this where two candidates' scores lie
+ * within its rounding of each other; the tests check such rows for validity
+ * against the fp64 scores (oracle_block_scores) instead of equality.
  * iq, ik: bf16 bit patterns [T][4][dim]; q2k: [4][T][16].
  */
-static float bf16_to_f32(uint16_t u) {
+static double bf16_to_f64(uint16_t u) {
   uint32_t w = (uint32_t)u << 16;
   float f;
   memcpy(&f, &w, sizeof f);
-  return f;
+  return (double)f;
 }
 
 /* (s1, v1) ranks before (s2, v2)? */
-static int sel_better(float s1, int32_t v1, float s2, int32_t v2) {
+static int sel_better(double s1, int32_t v1, double s2, int32_t v2) {
   return s1 > s2 || (s1 == s2 && v1 < v2);
+}
+
+/* summary(g, d, v)[0 .. dim) for every block v of document d. */
+static void block_summaries(const uint16_t* ik, int32_t dim, int64_t s0, int32_t len, int g,
+                            double* summ) {
+  const int32_t nb = nblocks(len);
+  for (int32_t v = 0; v < nb; ++v) {
+    const int32_t n = (len - v * BLK) < BLK ? (len - v * BLK) : BLK;
+    for (int32_t c = 0; c < dim; ++c) {
+      double acc = 0.0;
+      for (int32_t j = 0; j < n; ++j)
+        acc += bf16_to_f64(ik[((s0 + (int64_t)v * BLK + j) * NKV + g) * dim + c]);
+      summ[(int64_t)v * dim + c] = acc / (double)n;
+    }
+  }
+}
+
+/* score(t, g, v) for v = 0 .. b. */
+static void block_scores(const uint16_t* iq, int32_t dim, int64_t t, int g, int32_t b,
+                         const double* summ, double* score) {
+  for (int32_t v = 0; v <= b; ++v) {
+    double acc = 0.0;
+    for (int32_t c = 0; c < dim; ++c)
+      acc += bf16_to_f64(iq[(t * NKV + g) * dim + c]) * summ[(int64_t)v * dim + c];
+    score[v] = acc;
+  }
 }
 
 int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int32_t dim,
@@ -557,11 +582,11 @@ int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int3
   int64_t maxnb = 0;
   for (int32_t d = 0; d < D; ++d)
     if (nblocks(offs[d + 1] - offs[d]) > maxnb) maxnb = nblocks(offs[d + 1] - offs[d]);
-  int err = 0;
 #pragma omp parallel
   {
-    float* summ = (float*)malloc(sizeof(float) * (size_t)maxnb * (size_t)dim);
-    float* score = (float*)malloc(sizeof(float) * (size_t)maxnb);
+    double* summ = (double*)malloc(sizeof(double) * (size_t)maxnb * (size_t)dim);
+    double* score = (double*)malloc(sizeof(double) * (size_t)maxnb);
+    unsigned char* taken = (unsigned char*)malloc((size_t)maxnb);
     int32_t cached_doc = -1, cached_g = -1;
 #pragma omp for schedule(dynamic, 16)
     for (int64_t i = 0; i < 4 * T; ++i) {
@@ -570,34 +595,20 @@ int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int3
       const int32_t d = doc_of(offs, D, t);
       const int64_t s0 = offs[d];
       const int32_t len = offs[d + 1] - offs[d];
-      const int32_t nb = nblocks(len);
       const int32_t b = (int32_t)((t - s0) / BLK);
       int32_t* out = q2k + ((int64_t)g * T + t) * TOPK;
       if (b + 1 <= TOPK) {
         for (int k = 0; k < TOPK; ++k) out[k] = k <= b ? k : -1;
         continue;
       }
-      if (d != cached_doc || g != cached_g) { /* block summaries of (g, d) */
-        for (int32_t v = 0; v < nb; ++v) {
-          const int32_t n = (len - v * BLK) < BLK ? (len - v * BLK) : BLK;
-          for (int32_t c = 0; c < dim; ++c) {
-            float acc = 0.f;
-            for (int32_t j = 0; j < n; ++j)
-              acc += bf16_to_f32(ik[((s0 + (int64_t)v * BLK + j) * NKV + g) * dim + c]);
-            summ[(int64_t)v * dim + c] = acc / (float)n;
-          }
-        }
+      if (d != cached_doc || g != cached_g) {
+        block_summaries(ik, dim, s0, len, g, summ);
         cached_doc = d;
         cached_g = g;
       }
-      for (int32_t v = 0; v <= b; ++v) {
-        float acc = 0.f;
-        for (int32_t c = 0; c < dim; ++c)
-          acc = fmaf(bf16_to_f32(iq[(t * NKV + g) * dim + c]), summ[(int64_t)v * dim + c], acc);
-        score[v] = acc;
-      }
+      block_scores(iq, dim, t, g, b, summ, score);
       /* selection by repeated best-of-the-rest */
-      unsigned char* taken = (unsigned char*)calloc((size_t)b + 1, 1);
+      memset(taken, 0, (size_t)b + 1);
       int32_t chosen[TOPK];
       int nc = 0;
       if (force_local) {
@@ -613,7 +624,6 @@ int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int3
         taken[best] = 1;
         chosen[nc++] = best;
       }
-      free(taken);
       for (int x = 1; x < nc; ++x) /* ascending */
         for (int y = x; y > 0 && chosen[y - 1] > chosen[y]; --y) {
           int32_t tmp = chosen[y];
@@ -624,6 +634,55 @@ int oracle_select_blocks(const uint16_t* iq, const uint16_t* ik, int64_t T, int3
     }
     free(summ);
     free(score);
+    free(taken);
+  }
+  return OR_OK;
+}
+
+/* fp64 scores of the candidate blocks 0 .. b of the listed (index head,
+ * token) rows: scores[r * maxb + v] for v <= b, NaN after.  rows: n pairs
+ * (g, t), best sorted by (g, t) (a thread reuses the summaries of the last
+ * (g, document) it met); maxb: the row stride (>= largest b + 1). */
+int oracle_block_scores(const uint16_t* iq, const uint16_t* ik, int64_t T, int32_t dim,
+                        const int32_t* offs, int32_t D, const int64_t* rows, int64_t n,
+                        int64_t maxb, double* scores) {
+  if (T <= 0 || dim <= 0 || maxb <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  int64_t maxnb = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (nblocks(offs[d + 1] - offs[d]) > maxnb) maxnb = nblocks(offs[d + 1] - offs[d]);
+  int err = OR_OK;
+#pragma omp parallel
+  {
+    double* summ = (double*)malloc(sizeof(double) * (size_t)maxnb * (size_t)dim);
+    int32_t cached_doc = -1, cached_g = -1;
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t r = 0; r < n; ++r) {
+      const int g = (int)rows[2 * r];
+      const int64_t t = rows[2 * r + 1];
+      double* out = scores + r * maxb;
+      for (int64_t v = 0; v < maxb; ++v) out[v] = NAN;
+      if (g < 0 || g >= NKV || t < 0 || t >= T) {
+#pragma omp atomic write
+        err = OR_BAD_ARGS;
+        continue;
+      }
+      const int32_t d = doc_of(offs, D, t);
+      const int64_t s0 = offs[d];
+      const int32_t len = offs[d + 1] - offs[d];
+      const int32_t b = (int32_t)((t - s0) / BLK);
+      if (b + 1 > maxb) {
+#pragma omp atomic write
+        err = OR_BAD_ARGS;
+        continue;
+      }
+      if (d != cached_doc || g != cached_g) {
+        block_summaries(ik, dim, s0, len, g, summ);
+        cached_doc = d;
+        cached_g = g;
+      }
+      block_scores(iq, dim, t, g, b, summ, out);
+    }
+    free(summ);
   }
   return err;
 }

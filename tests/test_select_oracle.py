@@ -5,8 +5,10 @@
   * ties go to the lower block index;
   * queries whose document has at most 16 candidate blocks take them all;
   * on random inputs, the chosen blocks' scores (recomputed here in fp64 from
-    the bf16 values) all rank at or above every unchosen block, up to fp32
-    rounding, and the output is sorted, distinct and causal.
+    the bf16 values with numpy) all rank at or above every unchosen block, and
+    the output is sorted, distinct and causal;
+  * the oracle's per-candidate fp64 scores (used by the GPU validity test)
+    equal the same numpy recomputation.
 """
 import numpy as np
 import pytest
@@ -86,4 +88,26 @@ def test_random_selection_is_a_valid_top_k(oracle_mod):
                              for v in range(b + 1)])
             sc = summ @ qf[t, gg]
             unsel = [v for v in range(b + 1) if v not in sel]
-            assert sc[sel].min() >= sc[unsel].max() - 1e-4 * (1 + np.abs(sc).max())
+            assert sc[sel].min() >= sc[unsel].max() - 1e-12 * (1 + np.abs(sc).max())
+
+
+def test_block_scores_match_brute_force(oracle_mod):
+    g = torch.Generator().manual_seed(12)
+    lens = [700, 2900]
+    T = sum(lens)
+    iq = torch.randn(T, 4, DIM, generator=g).to(torch.bfloat16)
+    ik = torch.randn(T, 4, DIM, generator=g).to(torch.bfloat16)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rows = np.array([[0, 0], [1, 699], [2, 700], [3, 3599], [0, 2000], [2, 3000]])
+    sc = oracle_mod.block_scores(iq, ik, offs, rows)
+    qf, kf = iq.double().numpy(), ik.double().numpy()
+    for r, (gg, t) in enumerate(rows):
+        d = int(np.searchsorted(offs, t, side="right") - 1)
+        s0, n = int(offs[d]), int(lens[d])
+        b = (t - s0) // 128
+        for v in range(sc.shape[1]):
+            if v > b:
+                assert np.isnan(sc[r, v])
+                continue
+            summ = kf[s0 + 128 * v:s0 + min(n, 128 * v + 128), gg].mean(0)
+            assert abs(sc[r, v] - summ @ qf[t, gg]) <= 1e-12 * (1 + abs(sc[r, v]))
