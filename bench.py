@@ -169,7 +169,7 @@ def measure_packing(dev, peaks):
 def measure_selection(dev, peaks, dim: int = 64):
     """Block scorer + top-16 on the packed-document T=16384 row with index
     dim 64 (synthetic N(0,1) index queries / keys): device time per call and
-    the scoring FMA rate against the fp32 FMA peak (152 SMs x 128 lanes x the
+    the scoring FMA rate against the fp32 FMA peak (SMs x 128 lanes x the
     maximum SM clock)."""
     from block_sparse_gqa_msa_gb300 import api
     w = inputs.config(WORKLOAD)
@@ -203,7 +203,8 @@ def measure_selection(dev, peaks, dim: int = 64):
     api.msa_select_blocks(iq, ik, offs, q2k=q2k, workspace=ws)
     split = {k: api.profile_read(k)[1] for k in ("sel_summary", "sel_topk")}
     api.profile_enable(False)
-    peak = 152 * 128 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * 128 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
     return {"ms": ms, "fma": fma, "TFMA_s": fma / (ms * 1e-3) / 1e12,
             "frac_of_fp32_fma": fma / (ms * 1e-3) / peak, "bound": "alu",
             "kernels_ms": {k: round(v, 4) for k, v in split.items()},
@@ -314,7 +315,7 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
     q, k, v, do = (x.to(dev) for x in (w.q, w.k, w.v, w.do))
     q2k, offs = w.q2k.to(dev), w.doc_offsets.to(dev)
-    plan = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum)
+    plan = api.msa_build_plan(q2k, offs, super_block=args.super_block)
     pws = plan.workspace
     fws = torch.empty(api.forward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     bws = torch.empty(api.backward_workspace_bytes(plan), dtype=torch.uint8, device=dev)
@@ -324,7 +325,7 @@ def run_gpu(args, rank, world):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
-        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum,
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block,
                                  workspace=pws)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
         api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
@@ -356,7 +357,7 @@ def run_gpu(args, rank, world):
         flush.zero_()
         e = evs[i]
         e[0].record(stream)
-        p = api.msa_build_plan(q2k, offs, super_block=args.super_block, o_accum=args.o_accum,
+        p = api.msa_build_plan(q2k, offs, super_block=args.super_block,
                                  workspace=pws)
         e[1].record(stream)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
@@ -422,7 +423,7 @@ def run_gpu(args, rank, world):
                 stream.wait_event(out_done[b])
             qq, kk, vv, dd, q2, of = sets_in[b]
             oo, ll = sets_out[b][0], sets_out[b][1]
-            pp = api.msa_build_plan(q2, of, super_block=args.super_block, o_accum=args.o_accum,
+            pp = api.msa_build_plan(q2, of, super_block=args.super_block,
                                  workspace=pws)
             api.msa_forward(pp, qq, kk, vv, w.scale, o=oo, lse=ll, workspace=fws)
             api.msa_backward(pp, qq, kk, vv, oo, ll, dd, w.scale, dq=dq_, dk=dk_, dv=dv_,
@@ -470,7 +471,7 @@ def run_gpu(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "T": T, "docs": w.num_docs, "heads": "64q/4kv/4idx",
-                   "head_dim": 128, "block": 128, "topk": 16, "super_block": args.super_block, "o_pool": args.o_accum,
+                   "head_dim": 128, "block": 128, "topk": 16, "super_block": args.super_block, "o_pool": "f32",
                    "pairs": pairs, "flop_per_step": flop_step,
                    "l2": "flushed before each timed step (256 MiB write)"},
         "tokens_per_s": tok_s,
@@ -504,8 +505,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--super-block", type=int, default=64)
-    ap.add_argument("--o-accum", choices=["f32", "bf16"], default="f32",
-                    help="precision of the forward's O pool")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5],
                     help="synthetic workload (default: the packed 16k row the metric is quoted on)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

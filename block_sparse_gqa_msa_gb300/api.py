@@ -26,7 +26,7 @@ NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM, TOPK = 64, 4, 128, 16
 STATUS = {
     0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_ALIGNMENT",
     4: "MSA_ERR_WORKSPACE", 5: "MSA_ERR_CUDA", 6: "MSA_ERR_BAD_Q2K", 7: "MSA_ERR_BAD_OFFSETS",
-    8: "MSA_ERR_TIMEOUT", 9: "MSA_ERR_CAPACITY",
+    8: "MSA_ERR_TIMEOUT", 9: "MSA_ERR_CAPACITY", 10: "MSA_ERR_RANGE",
 }
 MSA_OK = 0
 
@@ -171,7 +171,8 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
                    dq_accum: str = "f16", o_accum: str = "f32") -> Plan:
     """Device-side plan from q2k int32 [4,T,16] and doc_offsets int32 [D+1].
     dq_accum: precision of the backward's dQ pool ("f16", "bf16" or "f32");
-    o_accum: precision of the forward's O pool ("f32" or "bf16")."""
+    o_accum: precision of the forward's O pool (only "f32" is accepted; the
+    library rejects "bf16", whose O error exceeds the forward's bar)."""
     if q2k.dim() != 3:
         raise ValueError("q2k must be [4, T, 16]")
     T = int(q2k.shape[1])

@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(256) k_bwd_delta(msa_plan p, const __nv_bfloat
                                                    const __nv_bfloat16* dO, float* delta,
                                                    uint4* dq_pool, int64_t dq_pool_vec,
                                                    float4* dkv_pool, int64_t dkv_vec) {
+  // the range warning describes one backward: start this one without it
+  if (blockIdx.x == 0 && threadIdx.x == 0) clear_warnings(p.header);
   if (plan_failed(p.header)) return;
   const int lane = threadIdx.x & 31;
   const int64_t rows = p.T * kQHeads;
@@ -727,7 +729,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ------------------------------------------------------------ bwd_finalize
 // Pools -> bf16 outputs.  dQ: one thread per (head octet of a token, 8 head
 // dimensions) reads the 64 interleaved pool values and writes 8 dims of each
-// of the octet's heads; dK / dV: 8 elements per thread.
+// of the octet's heads; dK / dV: 8 elements per thread.  A non-finite value
+// in a 16-bit dQ pool (fp16 saturates above 65504) sets MSA_ERR_RANGE.
 __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq_pool,
                                                       const float* dk_pool, const float* dv_pool,
                                                       __nv_bfloat16* dq, __nv_bfloat16* dk,
@@ -736,6 +739,7 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
   const int64_t nq = p.T * (kQHeads / 8) * (kHeadDim / 8);
   const int64_t nk8 = p.T * kKVHeads * kHeadDim / 8;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  uint32_t nonfinite = 0u;  // OR of the exponent fields that were all ones
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq + 2 * nk8;
        i += stride) {
     if (i < nq) {
@@ -768,6 +772,13 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
 #pragma unroll
           for (int h = 0; h < 8; ++h)
             out[h][e / 2] = pack_bf16x2(val(wa[h >> 1], h & 1), val(wb[h >> 1], h & 1));
+          if (f16) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              nonfinite |= ((wa[k] & 0x7C00u) == 0x7C00u) | ((wa[k] & 0x7C000000u) == 0x7C000000u);
+              nonfinite |= ((wb[k] & 0x7C00u) == 0x7C00u) | ((wb[k] & 0x7C000000u) == 0x7C000000u);
+            }
+          }
         }
       }
 #pragma unroll
@@ -784,6 +795,8 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
                      pack_bf16x2(b.z, b.w));
     }
   }
+  if (__any_sync(0xffffffffu, nonfinite != 0u) && (threadIdx.x & 31) == 0)
+    raise_status(p.header, MSA_ERR_RANGE);
 }
 
 }  // namespace

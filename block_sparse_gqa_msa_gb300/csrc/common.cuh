@@ -37,8 +37,14 @@ __device__ __forceinline__ void raise_status(int64_t* header, msa_status s) {
   atomicOr(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
            1ull << static_cast<int>(s));
 }
+// Status bits that are warnings about one call's result, not plan failures.
+constexpr int64_t kStatusWarnings = int64_t(1) << MSA_ERR_RANGE;
 __device__ __forceinline__ bool plan_failed(const int64_t* header) {
-  return *reinterpret_cast<const volatile int64_t*>(header + kHdrStatus) != 0;
+  return (*reinterpret_cast<const volatile int64_t*>(header + kHdrStatus) & ~kStatusWarnings) != 0;
+}
+__device__ __forceinline__ void clear_warnings(int64_t* header) {
+  atomicAnd(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
+            ~static_cast<unsigned long long>(kStatusWarnings));
 }
 
 // Per-document record in the plan: start token, length, blocks, first global block.

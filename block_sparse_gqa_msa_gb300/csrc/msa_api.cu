@@ -211,6 +211,7 @@ const char* msa_status_string(msa_status s) {
     case MSA_ERR_BAD_OFFSETS: return "MSA_ERR_BAD_OFFSETS";
     case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT";
     case MSA_ERR_CAPACITY: return "MSA_ERR_CAPACITY";
+    case MSA_ERR_RANGE: return "MSA_ERR_RANGE";
   }
   return "MSA_ERR_UNKNOWN";
 }
@@ -231,6 +232,10 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   const int32_t oacc = opts ? opts->o_accum : MSA_O_ACCUM_F32;
   if (Z < 0 || acc < MSA_DQ_ACCUM_F16 || acc > MSA_DQ_ACCUM_F32) return MSA_ERR_INVALID_ARG;
   if (oacc != MSA_O_ACCUM_F32 && oacc != MSA_O_ACCUM_BF16) return MSA_ERR_INVALID_ARG;
+  // A bf16 O pool rounds every partial sum to 8 bits and O once more on the
+  // store: up to one bf16 ulp of O (2^-6 for |O| in [2, 4)), above the 1e-2
+  // max-abs bar the forward is held to.  Not offered.
+  if (oacc == MSA_O_ACCUM_BF16) return MSA_ERR_UNSUPPORTED;
   if (!aligned16(q2k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(doc_offsets) & 3u))
     return MSA_ERR_ALIGNMENT;
   const PlanLayout L = plan_layout(T, num_docs);

@@ -63,7 +63,10 @@ typedef enum msa_status {
   MSA_ERR_BAD_Q2K = 6,      /* device: a q2k slot outside [-1, blocks of doc)  */
   MSA_ERR_BAD_OFFSETS = 7,  /* device: doc_offsets not 0 < ... strictly up .. T */
   MSA_ERR_TIMEOUT = 8,      /* device: a bounded pipeline wait gave up         */
-  MSA_ERR_CAPACITY = 9      /* device: a plan table exceeded its capacity      */
+  MSA_ERR_CAPACITY = 9,     /* device: a plan table exceeded its capacity      */
+  MSA_ERR_RANGE = 10        /* device warning: the last backward's 16-bit dQ
+                               pool overflowed (dQ holds inf / nan); rerun it
+                               with MSA_DQ_ACCUM_BF16 or MSA_DQ_ACCUM_F32      */
 } msa_status;
 
 /* Human-readable name of a status code (static string). */
@@ -71,7 +74,11 @@ const char* msa_status_string(msa_status s);
 
 /* Precision of the dQ accumulation pool of msa_backward.  The pages' default
  * is packed FP16 atomics with a BF16 switch for range (section "Supported
- * scope", the MSA_M3_DQ_ACCUM setting); FP32 is the widest and slowest. */
+ * scope", the MSA_M3_DQ_ACCUM setting); FP32 is the widest and slowest.
+ * FP16 saturates above 65504: when the finalize reads a non-finite FP16 pool
+ * value it sets MSA_ERR_RANGE in the plan's status word.  That bit is a
+ * warning about the last backward only (every backward clears it first) and,
+ * unlike the errors, does not make later kernels of the plan skip work. */
 typedef enum msa_dq_accum {
   MSA_DQ_ACCUM_F16 = 0,
   MSA_DQ_ACCUM_BF16 = 1,
@@ -80,9 +87,10 @@ typedef enum msa_dq_accum {
 
 /* Precision of the forward's O accumulation pool.  The up-to-16 block
  * partials of an output row are added in a pool at a shared row shift; FP32
- * keeps O's rounding to that of the final bf16 store, BF16 (same exponent
- * range) halves the pool's shared-memory staging, L2 reduction and HBM
- * traffic at the cost of an 8-bit mantissa in every addition. */
+ * keeps O's rounding to that of the final bf16 store.  MSA_O_ACCUM_BF16 is
+ * rejected with MSA_ERR_UNSUPPORTED: an 8-bit mantissa in every addition
+ * plus the bf16 store can put O one bf16 ulp (1.6e-2 at |O| in [2, 4)) off
+ * the exact result, above the forward's 1e-2 max-abs bar. */
 typedef enum msa_o_accum {
   MSA_O_ACCUM_F32 = 0,
   MSA_O_ACCUM_BF16 = 1
@@ -95,7 +103,7 @@ typedef struct msa_plan_options {
   int32_t super_block;
   /* An msa_dq_accum value.  Default MSA_DQ_ACCUM_F16. */
   int32_t dq_accum;
-  /* An msa_o_accum value.  Default (0) MSA_O_ACCUM_F32. */
+  /* An msa_o_accum value; only (0) MSA_O_ACCUM_F32 is accepted. */
   int32_t o_accum;
   int32_t reserved[5];
 } msa_plan_options;
@@ -181,8 +189,8 @@ msa_status msa_build_plan_static(const int32_t* q2k, const int32_t* doc_offsets,
                                  int32_t num_docs, const msa_plan_options* opts,
                                  msa_stream_t stream, msa_plan* out);
 
-/* Bytes of forward workspace for a plan (host only).  Dominated by the O
- * pool, T x 64 x 128 elements of the plan's o_accum type (4 or 2 bytes). */
+/* Bytes of forward workspace for a plan (host only).  Dominated by the fp32
+ * O pool, T x 64 x 128 x 4 bytes. */
 msa_status msa_forward_workspace_bytes(const msa_plan* plan, size_t* bytes);
 
 /*
@@ -213,7 +221,9 @@ msa_status msa_backward(const msa_plan* plan, const void* q, const void* k, cons
                         msa_stream_t stream);
 
 /* Synchronises the stream and returns the plan's device status (MSA_OK if no
- * device-side error was recorded).  For tests and diagnostics. */
+ * device-side error was recorded): the lowest-numbered error, else
+ * MSA_ERR_RANGE if the last backward's FP16 dQ pool overflowed.  For tests
+ * and diagnostics. */
 msa_status msa_read_status(const msa_plan* plan, msa_stream_t stream);
 
 /* Plan counts after synchronising the stream: counts[0] = key blocks NB,

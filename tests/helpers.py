@@ -15,16 +15,11 @@ def rel_fro(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm((got - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-30))
 
 
-# O accumulated in a bf16 pool (opt-in, msa_plan_options.o_accum): each value
-# is rounded to bf16 in the pool and again when O is stored, so the error can
-# reach one bf16 ulp instead of half of one: 2^-6 = 1.56e-2 for |O| in [2, 4).
-O_POOL16_MAX_ABS = 2e-2
 
-
-def check_o(got, ref, what="O", max_abs=O_MAX_ABS):
+def check_o(got, ref, what="O"):
     err = np.abs(got - ref).max() if got.size else 0.0
     rf = rel_fro(got, ref)
-    assert err <= max_abs and rf <= O_REL_FRO, f"{what}: max-abs {err:.3e}, rel-Fro {rf:.3e}"
+    assert err <= O_MAX_ABS and rf <= O_REL_FRO, f"{what}: max-abs {err:.3e}, rel-Fro {rf:.3e}"
 
 
 def check_lse(got, ref, what="LSE"):

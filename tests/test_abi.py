@@ -69,6 +69,10 @@ def test_build_plan_host_checks(lib):
                      api.MsaPlanOptions(super_block=16, o_accum=-1)):
         assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(bad_opts), good, ws_n.value,
                                   None, ctypes.byref(st)) == 1
+    # the bf16 O pool is not offered
+    assert lib.msa_build_plan(good, good, 1000, 2,
+                              ctypes.byref(api.MsaPlanOptions(super_block=16, o_accum=1)), good,
+                              ws_n.value, None, ctypes.byref(st)) == 2
     # alignment
     assert lib.msa_build_plan(ctypes.c_void_p(0x10004), good, 1000, 2, ctypes.byref(opts), good,
                               ws_n.value, None, ctypes.byref(st)) == 3
