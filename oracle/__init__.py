@@ -90,6 +90,8 @@ def _bind(lib):
     lib.oracle_select_blocks.argtypes = [_P, _P, _I64, _I32, _P, _I32, _I32, _P]
     lib.oracle_select_blocks.restype = ctypes.c_int
     lib.oracle_block_scores.argtypes = [_P, _P, _I64, _I32, _P, _I32, _P, _I64, _I64, _P]
+    lib.oracle_groups.argtypes = [_P, _I64, _P, _I32, _P, _P, _I64, _P]
+    lib.oracle_groups.restype = ctypes.c_int
     lib.oracle_block_scores.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
@@ -242,6 +244,36 @@ def plan(q2k, doc_offsets, T: int, super_block: int = 16, lib=None):
         "row_ptr": row_ptr[: 4 * NB + 1].copy(), "col": col[:nnz].copy(),
         "tasks": tasks[:nt].copy(),
     }
+
+
+def groups(q2k, doc_offsets, T: int, lib=None):
+    """Octet groups of the forward schedule (see oracle_groups in
+    msa_oracle.c): {"grouped": uint8 [4, T], "items": int64 [n, 22]} with item
+    rows (tokA, tokB or -1, nqA, nqB, g, nsel, 16 blocks ascending, -1 padded)."""
+    lib = lib or _load()
+    q2k = _i32(q2k)
+    offs = _i32(doc_offsets)
+    D = offs.size - 1
+    grouped = np.zeros((4, T), dtype=np.uint8)
+    cap = 4 * (T // 8 + D) + 4
+    items = np.zeros((cap, 22), dtype=np.int64)
+    counts = np.zeros(1, dtype=np.int64)
+    rc = lib.oracle_groups(_ptr(q2k), T, _ptr(offs), D, _ptr(grouped), _ptr(items), cap,
+                           _ptr(counts))
+    _check(rc, "groups")
+    return {"grouped": grouped, "items": items[:int(counts[0])].copy()}
+
+
+def forward_tasks(pl, grouped):
+    """The forward's task list: the plan's tasks (bucket, first col, count)
+    without those all of whose queries are grouped."""
+    NB, col = pl["NB"], pl["col"]
+    keep = []
+    for b, first, n in pl["tasks"]:
+        g = int(b) // NB
+        if not all(grouped[g, col[first:first + n]]):
+            keep.append((b, first, n))
+    return np.array(keep, dtype=np.int64).reshape(-1, 3)
 
 
 def pair_count(q2k, doc_offsets, T: int) -> int:

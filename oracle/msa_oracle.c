@@ -518,6 +518,110 @@ int oracle_threads(void) {
 }
 
 /* ------------------------------------------------------------------------
+ * Octet groups of the forward schedule (a reading: the pages fix the task
+ * tile - 8 queries x the 16 heads of an index head - but not how the tiles
+ * of one query set are merged).
+ *
+ * For index head g, the tokens of document d are cut into aligned octets:
+ * document positions 8k .. 8k+7 (fewer at the document's end).  An octet is
+ * GROUPED when all its tokens have the same non-empty set of visible
+ * selected blocks {v in q2k[g, t, :] : 0 <= v <= own block} (all tokens of an
+ * octet share their block).  A grouped octet's rows see exactly its blocks,
+ * so one tile can accumulate them block after block without a merge.
+ * Grouped octets at positions 16k and 16k+8 of one document with the same
+ * set form one item; every other grouped octet is an item alone.
+ *   grouped: uint8 [4][T]  (1 = the token's octet is grouped)
+ *   items:   int64 [cap][6 + 16]: tokA, tokB (-1 if none), nqA, nqB, g,
+ *            nsel, blocks ascending (-1 padded); items in (g, d, k) order
+ *   counts:  [0] = items
+ * The forward's task list is then the task list without the tasks all of
+ * whose queries are grouped (see oracle/__init__.py).
+ */
+int oracle_groups(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D,
+                  unsigned char* grouped, int64_t* items, int64_t item_cap, int64_t* counts) {
+  if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+  if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
+  int32_t maxnb = 0;
+  for (int32_t d = 0; d < D; ++d)
+    if (nblocks(offs[d + 1] - offs[d]) > maxnb) maxnb = nblocks(offs[d + 1] - offs[d]);
+  unsigned char* s0 = (unsigned char*)malloc((size_t)maxnb);
+  unsigned char* s1 = (unsigned char*)malloc((size_t)maxnb);
+  memset(grouped, 0, (size_t)(4 * T));
+  int64_t n = 0;
+  int rc = OR_OK;
+  for (int g = 0; g < NKV && !rc; ++g)
+    for (int32_t d = 0; d < D && !rc; ++d) {
+      const int64_t st = offs[d];
+      const int32_t len = offs[d + 1] - offs[d];
+      const int32_t nb = nblocks(len);
+      /* octet k covers document positions [8k, min(8k + 8, len)) */
+      const int32_t noct = (len + 7) / 8;
+      int32_t* oct_nsel = (int32_t*)malloc(sizeof(int32_t) * (size_t)noct);
+      for (int32_t k = 0; k < noct; ++k) {
+        const int64_t t0 = st + 8 * (int64_t)k;
+        const int64_t t1 = (8 * (int64_t)k + 8 < len) ? t0 + 8 : st + len;
+        const int32_t b = (int32_t)(8 * (int64_t)k / BLK);
+        selection(q2k, T, g, t0, nb, s0);
+        int32_t nsel = 0;
+        for (int32_t v = 0; v <= b; ++v) nsel += s0[v];
+        int same = nsel > 0;
+        for (int64_t t = t0 + 1; t < t1 && same; ++t) {
+          selection(q2k, T, g, t, nb, s1);
+          for (int32_t v = 0; v <= b; ++v)
+            if (s1[v] != s0[v]) same = 0;
+        }
+        oct_nsel[k] = same ? nsel : 0;
+        if (same)
+          for (int64_t t = t0; t < t1; ++t) grouped[(int64_t)g * T + t] = 1;
+      }
+      for (int32_t k = 0; k < noct && !rc; ++k) {
+        if (!oct_nsel[k]) continue;
+        const int64_t t0 = st + 8 * (int64_t)k;
+        const int32_t b = (int32_t)(8 * (int64_t)k / BLK);
+        int pair = 0;
+        if (k % 2 == 0 && k + 1 < noct && oct_nsel[k + 1]) {
+          selection(q2k, T, g, t0, nb, s0);
+          selection(q2k, T, g, t0 + 8, nb, s1);
+          pair = 1;
+          for (int32_t v = 0; v <= b; ++v)
+            if (s0[v] != s1[v]) pair = 0;
+        }
+        if (k % 2 == 1 && oct_nsel[k - 1]) { /* partner of an even octet? */
+          selection(q2k, T, g, t0 - 8, nb, s0);
+          selection(q2k, T, g, t0, nb, s1);
+          int same = 1;
+          for (int32_t v = 0; v <= b; ++v)
+            if (s0[v] != s1[v]) same = 0;
+          if (same) continue; /* already in the even octet's item */
+        }
+        if (n >= item_cap) {
+          rc = OR_CAPACITY;
+          break;
+        }
+        int64_t* it = items + n * 22;
+        const int32_t nqa = (8 * k + 8 < len) ? 8 : len - 8 * k;
+        it[0] = t0;
+        it[1] = pair ? t0 + 8 : -1;
+        it[2] = nqa;
+        it[3] = pair ? ((8 * (k + 1) + 8 < len) ? 8 : len - 8 * (k + 1)) : 0;
+        it[4] = g;
+        it[5] = oct_nsel[k];
+        selection(q2k, T, g, t0, nb, s0);
+        int32_t j = 0;
+        for (int32_t v = 0; v <= b; ++v)
+          if (s0[v]) it[6 + j++] = v;
+        for (; j < TOPK; ++j) it[6 + j] = -1;
+        ++n;
+      }
+      free(oct_nsel);
+    }
+  counts[0] = n;
+  free(s0);
+  free(s1);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------
  * Block selection: the index scorer and top-k that produce q2k.
  *
  * The pages name the step (an indexer scores the key blocks, each query
