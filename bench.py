@@ -38,6 +38,10 @@ FWD_FLOP_PER_PAIR = 4 * HEAD_DIM
 BWD_FLOP_PER_PAIR = 10 * HEAD_DIM
 METRIC = "MSA fwd+bwd sparse TFLOP/s & tokens/s at T=16k; % of GB300 BF16 tensor peak"
 WORKLOAD = 3  # packed 16k row of documents
+# every kernel family the library launches on the plan / forward / backward path
+KERNELS = ("plan_docs", "plan_count", "plan_scan", "plan_scatter", "plan_emit", "plan_ftasks",
+           "fwd_kmax", "fwd_v16", "fwd_rows", "fwd_group", "fwd_main", "fwd_finalize",
+           "fwd_fallback", "bwd_delta", "bwd_main", "bwd_finalize")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -368,9 +372,7 @@ def run_gpu(args, rank, world):
     launches = api.launch_count() - launches0
     clk = clocks.stop() if clocks else None
     kern = {}
-    for name in ("plan_docs", "plan_count", "plan_scan", "plan_scatter", "plan_emit", "fwd_kmax",
-                 "fwd_rows", "fwd_main", "fwd_finalize", "fwd_fallback", "bwd_delta", "bwd_main",
-                 "bwd_finalize"):
+    for name in KERNELS:
         n, ms = api.profile_read(name)
         if n:
             kern[name] = {"launches": n, "ms_per_step": ms / args.steps}

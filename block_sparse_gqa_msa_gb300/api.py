@@ -47,6 +47,8 @@ class MsaPlanStruct(ctypes.Structure):
         ("off", ctypes.c_void_p), ("col", ctypes.c_void_p), ("tcnt", ctypes.c_void_p),
         ("toff", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("scan_tmp", ctypes.c_void_p),
         ("scan_tmp_len", ctypes.c_int64),
+        ("item_cap", ctypes.c_int64), ("grouped", ctypes.c_void_p), ("items", ctypes.c_void_p),
+        ("fflag", ctypes.c_void_p), ("fpos", ctypes.c_void_p), ("ftasks", ctypes.c_void_p),
     ]
 
 
@@ -83,6 +85,7 @@ SIGNATURES = {
     "msa_read_status": ([_PLAN, _P], _I32),
     "msa_plan_counts": ([_PLAN, _P, ctypes.POINTER(_I64)], _I32),
     "msa_plan_export": ([_PLAN, _P, _P, _I64, _P, _I64], _I32),
+    "msa_plan_export_groups": ([_PLAN, _P, _P, _I64, _P, _I64, _P, _I64], _I32),
     "msa_profile_enable": ([_I32], _I32),
     "msa_profile_reset": ([], _I32),
     "msa_profile_read": ([ctypes.c_char_p, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double)],
@@ -270,9 +273,10 @@ def msa_read_status(plan: Plan, stream=None) -> int:
 
 
 def msa_plan_counts(plan: Plan, stream=None) -> dict:
-    c = (_I64 * 5)()
+    c = (_I64 * 7)()
     _check(lib().msa_plan_counts(plan.ref(), _stream(stream), c), "msa_plan_counts")
-    return {"NB": c[0], "nnz": c[1], "ntasks": c[2], "pairs": c[3], "entries": c[4]}
+    return {"NB": c[0], "nnz": c[1], "ntasks": c[2], "pairs": c[3], "entries": c[4],
+            "items": c[5], "ftasks": c[6]}
 
 
 def msa_plan_export(plan: Plan, stream=None):
@@ -283,6 +287,21 @@ def msa_plan_export(plan: Plan, stream=None):
     _check(lib().msa_plan_export(plan.ref(), _stream(stream), col.ctypes.data_as(_P), col.size,
                                  tasks.ctypes.data_as(_P), tasks.shape[0]), "msa_plan_export")
     return col[:cnt["nnz"]], tasks[:cnt["ntasks"]]
+
+
+def msa_plan_export_groups(plan: Plan, stream=None):
+    """(grouped uint8 [4, T], items int32 [n_items, 20], ftasks int32
+    [n_ftasks, 4]) - the forward's octet groups - copied to host."""
+    cnt = msa_plan_counts(plan, stream)
+    T = plan.struct.T
+    grouped = np.zeros((4, T), dtype=np.uint8)
+    items = np.zeros((max(cnt["items"], 1), 20), dtype=np.int32)
+    ftasks = np.zeros((max(cnt["ftasks"], 1), 4), dtype=np.int32)
+    _check(lib().msa_plan_export_groups(plan.ref(), _stream(stream), grouped.ctypes.data_as(_P),
+                                        T, items.ctypes.data_as(_P), items.shape[0],
+                                        ftasks.ctypes.data_as(_P), ftasks.shape[0]),
+           "msa_plan_export_groups")
+    return grouped, items[:cnt["items"]], ftasks[:cnt["ftasks"]]
 
 
 def profile_enable(on: bool = True):

@@ -2,28 +2,35 @@
 //
 // The method (NeMo-Automodel PR "feat(minimax-m3): add SM100 MSA sparse
 // attention with custom backward", section "Design": the flat forward
-// O[T,64,128] from the CSR / schedule) is computed KV-parallel: every task is
-// one 128-row tile (8 queries x 16 heads of one index head) against one
-// 128-key block, so K/V stay resident in shared memory across the tasks of a
-// bucket and each tile is a dense 128x128x128 tensor-core contraction.
+// O[T,64,128] from the CSR / schedule) is computed on 128-row tiles (8
+// queries x 16 heads of one index head) against one 128-key block, each a
+// dense 128x128x128 tensor-core contraction.
 //
-// The up-to-16 partial results of a row (one per selected block) are merged
-// without a second pass over the scores.  Each task exponentiates against its
-// own tile row maximum m (P = exp(s - m) in (0, 1], fp16 for the P.V product)
-// and rescales its partial P.V and row sum by exp(m - M) onto a per-row shift
-// M[t,h] shared by all tasks of the row: the Cauchy-Schwarz bound
-// scale * |q_th| * max_{selected v} max_{j in v} |k_jg| on every score of the
-// row, lowered by a fixed headroom so that a loose bound (a few keys of large
-// norm) does not push the sum towards underflow.  The rescaled partials add up
-// in fp32 pools with L2 bulk reductions; the finalize divides.  Rows whose sum
-// still underflows (the bound more than headroom + 60 octaves above the true
-// maximum) are recomputed exactly by a fallback kernel.
+// Every row (token, head) gets a shift M shared by all its tiles: the
+// Cauchy-Schwarz bound scale * |q_th| * max_{selected v} max_{j in v} |k_jg|
+// on its scores, lowered by a fixed headroom so that a loose bound (a few
+// keys of large norm) does not push the sum towards underflow.  Tiles
+// exponentiate against it, P = exp(s - M) as bf16 (same exponent range as
+// fp32), so the partials P.V and row sums of a row add up plainly, in any
+// order, without a second pass over the scores and without rescaling.
+//
+// Two schedules share that arithmetic:
+//   * grouped octets (8 consecutive tokens of a document whose tokens see the
+//     same blocks; the plan finds them): one CTA takes the octet (with a
+//     second one of the same blocks) and walks its blocks, the tile's O
+//     accumulating in tensor memory - written out once, no pool;
+//   * every other query: KV-parallel tasks, K/V resident in shared memory
+//     across the tasks of a bucket; the partials go to an fp32 pool with L2
+//     bulk reductions, and the finalize divides.
+// Rows whose sum still underflows (the bound more than headroom + 60
+// octaves above the true maximum) are recomputed exactly by a fallback.
 //
 // Kernels, in launch order:
-//   fwd_kmax      per (index head, key block): max key norm
-//   fwd_rows      per (token, index head): row shifts M, zero the pools
-//   fwd_main      the tensor-core tile loop (TMA + tcgen05 + TMEM)
-//   fwd_finalize  O = pool / sum -> bf16, LSE; flags underflowed rows
+//   fwd_kmax      per (index head, key block): max key norm, max |v|
+//   fwd_rows      per ungrouped (token, index head): row shifts M, zero the pool
+//   fwd_group     grouped octets: block walk with O in tensor memory
+//   fwd_main      the pooled task loop (TMA + tcgen05 + TMEM)
+//   fwd_finalize  pooled rows: O = pool / sum -> bf16, LSE; flags underflow
 //   fwd_fallback  exact recomputation of the flagged rows (usually none)
 #include "common.cuh"
 #include "sm100.cuh"
@@ -37,11 +44,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kUnderflowSum = 8.673617379884035e-19f;
 
 // ------------------------------------------------------------ workspace
-// Bytes per element of the O pool (fp32, or bf16 on request).
-inline size_t pool_elem_bytes(const msa_plan& p) { return p.o_accum == MSA_O_ACCUM_BF16 ? 2 : 4; }
 
 struct FwdLayout {
-  size_t off_m, off_l, off_pool, off_kmax, off_vmax, off_list, total;
+  size_t off_m, off_l, off_pool, off_kmax, off_vmax, off_list, off_v16, off_vscale, total;
 };
 FwdLayout fwd_layout(const msa_plan& p) {
   FwdLayout L{};
@@ -49,21 +54,14 @@ FwdLayout fwd_layout(const msa_plan& p) {
   size_t o = 0;
   L.off_m = o;    o = align_up(o + sizeof(float) * rows, 256);
   L.off_l = o;    o = align_up(o + sizeof(float) * rows, 256);
-  L.off_pool = o; o = align_up(o + pool_elem_bytes(p) * rows * kHeadDim, 256);
+  L.off_pool = o; o = align_up(o + sizeof(float) * rows * kHeadDim, 256);
   L.off_kmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
   L.off_vmax = o; o = align_up(o + sizeof(float) * kKVHeads * p.nb_cap, 256);
   L.off_list = o; o = align_up(o + sizeof(int32_t) * (rows + 1), 256);
+  L.off_v16 = o;  o = align_up(o + sizeof(uint16_t) * p.T * kKVHeads * kHeadDim, 256);
+  L.off_vscale = o; o = align_up(o + sizeof(float) * kKVHeads, 256);
   L.total = o;
   return L;
-}
-
-// V tiles enter the P.V product as fp16.  A block whose largest |v| exceeds
-// 2^15 is scaled by an exact power of two 2^-e first; the epilogue multiplies
-// by 2^e.  Returns 2^-e (1 for every ordinary block).
-__device__ __forceinline__ float v_scale_in(float vmax) {
-  if (!(vmax > 32768.f)) return 1.f;
-  const int e = int(ceilf(log2f(vmax * (1.f / 32768.f))));
-  return __int_as_float((127 - (e < 126 ? e : 126)) << 23);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -147,10 +145,55 @@ __global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat1
   }
 }
 
-// ------------------------------------------------------------ fwd_rows
-// One warp per (token, index head): the shift M2 of each of the 16 heads'
-// rows (-inf when the row sees no key), and zero the row's pool and sum.
-//
+// ------------------------------------------------------------ fwd_v16
+// V as fp16 for the P.V products (P is fp16, and one tensor-core product
+// takes one operand type).  fp16 holds |v| up to 65504, so every value of
+// KV head g is scaled by 2^-e_g, e_g the smallest exponent that brings g's
+// largest |v| to at most 2^15 (0 for ordinary data, where the copy is exact);
+// the kernels multiply O by vscale[g] = 2^e_g.
+__device__ __forceinline__ float v_scale_in(float vmax) {
+  if (!(vmax > 32768.f)) return 1.f;
+  const int e = int(ceilf(log2f(vmax * (1.f / 32768.f))));
+  return __int_as_float((127 - (e < 126 ? e : 126)) << 23);
+}
+__global__ void __launch_bounds__(256) k_fwd_v16(msa_plan p, const __nv_bfloat16* V,
+                                                 const float* vmax, uint4* v16, float* vscale) {
+  __shared__ float red[8][4];
+  if (plan_failed(p.header)) return;
+  const int64_t NB = p.header[kHdrNB];
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int64_t i = threadIdx.x; i < NB; i += blockDim.x)
+#pragma unroll
+    for (int g = 0; g < 4; ++g) m[g] = fmaxf(m[g], vmax[int64_t(g) * p.nb_cap + i]);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
+    if (lane == 0) red[w][g] = m[g];
+  }
+  __syncthreads();
+  float sc[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float x = red[0][g];
+    for (int k = 1; k < int(blockDim.x >> 5); ++k) x = fmaxf(x, red[k][g]);
+    sc[g] = v_scale_in(x);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < 4) vscale[threadIdx.x] = 1.f / sc[threadIdx.x];
+  const int64_t n = p.T * kKVHeads * kHeadDim / 8;  // 16-byte chunks, 16 per (token, head)
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const float f = sc[(i >> 4) & 3];
+    const uint4 x = reinterpret_cast<const uint4*>(V)[i];
+    v16[i] = make_uint4(pack_f16x2(bf16_lo(x.x) * f, bf16_hi(x.x) * f),
+                        pack_f16x2(bf16_lo(x.y) * f, bf16_hi(x.y) * f),
+                        pack_f16x2(bf16_lo(x.z) * f, bf16_hi(x.z) * f),
+                        pack_f16x2(bf16_lo(x.w) * f, bf16_hi(x.w) * f));
+  }
+}
+
+// ------------------------------------------------------------ row shifts
 // The Cauchy-Schwarz bound B = c2 * |q_th| * kmax_sel (log2 units) is never
 // below the row's true maximum m, but may sit far above it (a few keys of
 // large norm).  The shift is placed H below it, M2 = B - H, so that the row's
@@ -159,15 +202,29 @@ __global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat1
 // 2^H * 2^11 * vmax_sel (2048 keys, P <= 1): H = 64, lowered for rows whose
 // selected blocks hold |v| above 2^48, keeps that below 2^124.
 constexpr float kShiftHeadroom = 64.f;
+// km: max key norm over the row's visible selected blocks (< 0: none);
+// vm: their max |v| (may be inf or nan for non-finite V: no headroom then).
+__device__ __forceinline__ float row_shift(float c2, float qnorm, float km, float vm) {
+  const float headroom =
+      (vm <= 281474976710656.f) ? kShiftHeadroom
+                                : (vm < INFINITY ? fmaxf(0.f, 112.f - ceilf(log2f(vm))) : 0.f);
+  return km < 0.f ? -INFINITY : c2 * qnorm * km - headroom;
+}
+
+// ------------------------------------------------------------ fwd_rows
+// One warp per ungrouped (token, index head): the shift M2 of each of the 16
+// heads' rows (-inf when the row sees no key), and zero the row's pool and
+// sum.  Grouped rows are the group kernel's alone.
 __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat16* Q,
                                                   const float* kmax, const float* vmax,
                                                   float c2, float* M2, float* lsum,
-                                                  uint8_t* pool, int pool_esz) {
+                                                  float* pool) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
   const int64_t t = wid >> 2;
   const int g = int(wid & 3);
+  if (p.grouped[int64_t(g) * p.T + t]) return;
   const int d = doc_of_token(p.doc_offsets, p.num_docs, t);
   const DocInfo di = reinterpret_cast<const DocInfo*>(p.doc_info)[d];
   const int64_t qb = (t - di.start) / kBlock;
@@ -184,13 +241,9 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
     km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
   }
-  // vm may be inf or nan (non-finite V): no headroom then.
-  const float headroom =
-      (vm <= 281474976710656.f) ? kShiftHeadroom
-                                : (vm < INFINITY ? fmaxf(0.f, 112.f - ceilf(log2f(vm))) : 0.f);
   // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
   const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-  uint8_t* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim * pool_esz;
+  float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
   const int half = lane >> 4, sub = lane & 15;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
@@ -208,90 +261,23 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
     for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (sub == 0) {
       const int64_t row = t * kQHeads + g * kHeadsPerGroup + hh;
-      M2[row] = km < 0.f ? -INFINITY : c2 * sqrtf(s) * km - headroom;
+      M2[row] = row_shift(c2, sqrtf(s), km, vm);
       lsum[row] = 0.f;
     }
   }
-  uint4* z = reinterpret_cast<uint4*>(prow);
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  const int n16 = kHeadsPerGroup * kHeadDim * pool_esz / 16;
+  float4* z = reinterpret_cast<float4*>(prow);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int i = lane; i < n16; i += 32) z[i] = zero;
+  for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
 }
 
-// ------------------------------------------------------------ fwd_main
-// Warp roles (480 threads):
-//   0     TMA producer: K/V per block run, Q per task (two stages)
-//   1     MMA issuer (TMEM owner): S = Q K^T, O_part = P V with P read from TMEM
-//   2-9   softmax (thread = tile row = TMEM lane): row max, P = exp(s - m) as
-//         fp16 into the stage's P columns, row sum; warps 2-5 take the even
-//         tasks (TMEM stage 0), warps 6-9 the odd ones (stage 1)
-//   10-13 epilogue (thread = tile row): O_part * exp(m - M) staged in shared
-//         memory and added to the fp32 pool by bulk tensor reductions (four
-//         2 KB boxes per query, issued by one lane per warp); row sums by
-//         atomics
-//   14    V tile bf16 -> fp16 (power-of-two scaled when |v| is large)
-// TMEM: S in two stages, P (fp16) of each stage in columns of its own, one
-// O_part stage (see kTmP0, kTmO).
-constexpr int kFwdThreads = 480;
+// ------------------------------------------------------------ shared pieces
 constexpr uint32_t kTileBytes = 32768;
-constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
-// Epilogue staging: per query of the tile, four 2 KB boxes (16 heads x 32
-// columns, fp32, 128-byte swizzle) - the boxes of the pool's tensor map.
-constexpr uint32_t kStageBytes = kTaskQueries * 8192;
-constexpr uint32_t kFwdSmem = kSmStage + kStageBytes + 1024;
 
-// TMEM columns: S in two stages [0,128) and [128,256); P of stage st (fp16
-// pairs) in [256 + 64 st, 320 + 64 st); one O_part stage [384,512).  P has
-// columns of its own so that S(t+2) can overwrite S(t) as soon as the
-// softmax has read it, without waiting for P(t).V.
-constexpr uint32_t kTmP0 = 256, kTmO = 384;
-
-struct FwdBars {
-  uint64_t kv_full, kv_empty, v_ready, q_full[2], q_empty[2], s_full[2], s_free[2], p_full[2],
-      pv_done[2], rs_free[2], o_full, o_free, fin;
-};
-
-struct FwdParams {
-  msa_plan plan;
-  const float* M2;
-  const float* vmax;
-  void* pool;
-  float* lsum;
-  float c2;
-};
-
-// Task i of the CTA's walk: chunks of kFwdChunk consecutive tasks go round-robin
-// over the CTAs, so all CTAs advance through the task list together.
-// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
-// index arithmetic runs on the MMA issuer's critical path).
-constexpr int kFwdChunk = 16;
-__device__ __forceinline__ int64_t cta_task(int64_t i) {
-  return (int64_t(blockIdx.x) + (i / kFwdChunk) * gridDim.x) * kFwdChunk + (i % kFwdChunk);
-}
-__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
-  constexpr int chunk = kFwdChunk;
-  const int64_t nchunks = (ntasks + chunk - 1) / chunk;
-  if (int64_t(blockIdx.x) >= nchunks) return 0;
-  const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;  // chunks of this CTA
-  const int64_t last_chunk = blockIdx.x + (mine - 1) * gridDim.x;
-  return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
-                                                                    : chunk);
-}
-// Task record i of this CTA's walk; past the end, the last one (every
-// caller guards its uses by the index).  Only the address depends on the
-// index test, never the loaded value, so nothing waits for the load until
-// the record is used.  With no tasks, entry 0 of the (allocated) table.
-__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
-  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
-}
-__device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
-  return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
-}
-
-// Softmax of one tile row held in TMEM columns [cs, cs + 128) of the
-// thread's lane: keys after jmax are excluded when MASK (diagonal and partial
-// blocks, padded queries with jmax = -1).
+// Maximum raw score of one tile row held in TMEM columns [cs, cs + 128) of
+// the thread's lane over its visible keys (keys after jmax are excluded when
+// MASK: diagonal and partial blocks, rows with jmax = -1); 16 columns load
+// while the previous 16 are reduced.
 template <bool MASK>
 __device__ __forceinline__ float tile_row_max(uint32_t cs, int jmax) {
   float m[4];
@@ -312,8 +298,6 @@ __device__ __forceinline__ float tile_row_max(uint32_t cs, int jmax) {
   tmem_ld16(cs, r0);
   tmem_ld_wait();
   reg_fence16(r0);
-  // 16-column chunks 2i (r0) and 2i+1 (r1); the next chunk loads while the
-  // current one is reduced
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
     tmem_ld16(cs + 32 * i + 16, r1);
@@ -330,15 +314,19 @@ __device__ __forceinline__ float tile_row_max(uint32_t cs, int jmax) {
   return fmaxf(fmax3(m[0], m[1], m[2]), m[3]);
 }
 
-// P = 2^(s c2 - mxc) written as fp16 pairs over the columns already read
-// (columns [cs + 8c, cs + 8c + 8) after reading [cs + 16c, cs + 16c + 16));
-// the next 16 columns are loaded while the current ones are exponentiated.
-// Returns the row sum of the fp32 values.
+// P = 2^(s c2 - mref) of one tile row held in TMEM columns [cs, cs + 128),
+// written as fp16 pairs to columns [cp, cp + 64): columns [cp + 8c,
+// cp + 8c + 8) after reading [cs + 16c, cs + 16c + 16), the next 16 columns
+// loading while the current ones are exponentiated (cp may equal cs: a chunk
+// only overwrites columns already read).  mref is at or above the row's
+// scores less 8 octaves, so P <= 2^8 fits fp16 with an 11-bit significand.
+// Keys after jmax get P = 0 when MASK.  Returns the row sum of the fp32
+// values.
 template <bool MASK>
 __device__ __forceinline__ float tile_row_exp(uint32_t cs, uint32_t cp, int jmax, float c2,
-                                             float mxc) {
+                                             float mref) {
   const uint64_t cc = f2_pack(__float_as_uint(c2), __float_as_uint(c2));
-  const uint64_t nm = f2_pack(__float_as_uint(-mxc), __float_as_uint(-mxc));
+  const uint64_t nm = f2_pack(__float_as_uint(-mref), __float_as_uint(-mref));
   uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
   auto expo = [&](const uint32_t (&r)[16], int lim, uint32_t dst) {
     uint32_t pk[8];
@@ -377,6 +365,103 @@ __device__ __forceinline__ float tile_row_exp(uint32_t cs, uint32_t cp, int jmax
   return f2_lo(s2) + f2_hi(s2);
 }
 
+// Loads the 8 queries x 16 heads of one index head (two 16 KB column halves,
+// 128-byte swizzled) into a tile: one {64 cols, 16 rows} box per query and half.
+__device__ __forceinline__ void load_q_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            const int32_t (&tok)[kTaskQueries], int g) {
+#pragma unroll
+  for (int qi = 0; qi < kTaskQueries; ++qi) {
+    const int y = tok[qi] * kQHeads + g * kHeadsPerGroup;
+    tma_load_2d(dst + qi * 2048, map, bar, 0, y);
+    tma_load_2d(dst + 16384 + qi * 2048, map, bar, 64, y);
+  }
+}
+// K and V of one key block of KV head g (keys past T read as zero).
+__device__ __forceinline__ void load_kv_tiles(uint32_t dk, uint32_t dv, const CUtensorMap* mk,
+                                              const CUtensorMap* mv, uint32_t bar, int g,
+                                              int key_start) {
+  tma_load_3d(dk, mk, bar, 0, g, key_start);
+  tma_load_3d(dk + 16384, mk, bar, 64, g, key_start);
+  tma_load_3d(dv, mv, bar, 0, g, key_start);
+  tma_load_3d(dv + 16384, mv, bar, 64, g, key_start);
+}
+
+// ------------------------------------------------------------ fwd_main
+// The pooled tasks (the plan's forward list: tasks with at least one
+// ungrouped query; grouped queries in them are masked).
+// Warp roles (448 threads):
+//   0     TMA producer: K/V per block run, Q per task (two stages)
+//   1     MMA issuer (TMEM owner): S = Q K^T, O_part = P V with P read from TMEM
+//   2-9   softmax (thread = tile row = TMEM lane): row max m over the tile,
+//         P = exp(s - m) as fp16 (the maximum is exactly 1) into the stage's
+//         P columns, row sum; warps 2-5 take the even tasks (TMEM stage 0),
+//         warps 6-9 the odd ones (stage 1)
+//   10-13 epilogue (thread = tile row): O_part * exp(m - M) staged in shared
+//         memory and added to the fp32 pool by bulk tensor reductions (four
+//         2 KB boxes per query, issued by one lane per warp); row sums by
+//         atomics
+// TMEM: S in two stages, P (fp16) of each stage in columns of its own, one
+// O_part stage (see kTmP0, kTmO).  V tiles come from the forward's fp16 copy.
+constexpr int kFwdThreads = 448;
+constexpr uint32_t kSmK = 0, kSmV = 32768, kSmQ = 65536, kSmStage = 131072;
+// Epilogue staging: per query of the tile, four 2 KB boxes (16 heads x 32
+// columns, fp32, 128-byte swizzle) - the boxes of the pool's tensor map.
+constexpr uint32_t kStageBytes = kTaskQueries * 8192;
+constexpr uint32_t kFwdSmem = kSmStage + kStageBytes + 1024;
+
+// TMEM columns: S in two stages [0,128) and [128,256); P of stage st (fp16
+// pairs) in [256 + 64 st, 320 + 64 st); one O_part stage [384,512).  P has
+// columns of its own so that S(t+2) can overwrite S(t) as soon as the
+// softmax has read it, without waiting for P(t).V.
+constexpr uint32_t kTmP0 = 256, kTmO = 384;
+
+struct FwdBars {
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], s_free[2], p_full[2],
+      pv_done[2], rs_free[2], o_full, o_free, fin;
+};
+
+struct FwdParams {
+  msa_plan plan;
+  const float* M2;
+  const float* kmax;
+  const float* vmax;
+  float* pool;
+  float* lsum;
+  int32_t* list;  // fallback rows: [0] count, then rows
+  __nv_bfloat16* O;
+  float* lse;
+  const float* vscale;  // per KV head: 2^e of the fp16 V copy
+  float c2;
+};
+
+// Task i of the CTA's walk: chunks of kFwdChunk consecutive tasks go round-robin
+// over the CTAs, so all CTAs advance through the task list together.
+// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
+// index arithmetic runs on the MMA issuer's critical path).
+constexpr int kFwdChunk = 16;
+__device__ __forceinline__ int64_t cta_task(int64_t i) {
+  return (int64_t(blockIdx.x) + (i / kFwdChunk) * gridDim.x) * kFwdChunk + (i % kFwdChunk);
+}
+__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
+  constexpr int chunk = kFwdChunk;
+  const int64_t nchunks = (ntasks + chunk - 1) / chunk;
+  if (int64_t(blockIdx.x) >= nchunks) return 0;
+  const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;  // chunks of this CTA
+  const int64_t last_chunk = blockIdx.x + (mine - 1) * gridDim.x;
+  return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
+                                                                    : chunk);
+}
+// Task record i of this CTA's walk; past the end, the last one (every
+// caller guards its uses by the index).  Only the address depends on the
+// index test, never the loaded value, so nothing waits for the load until
+// the record is used.  With no tasks, entry 0 of the (allocated) table.
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
+  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
+}
+__device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
+  return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
+}
+
 // MMA issuer of k_fwd_main (one thread).  A function of its own so its few
 // live values stay in registers whatever the other roles need.
 __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t sbase,
@@ -397,7 +482,7 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
   auto kstep = [](int kk) { return uint64_t((kk >> 2) * 1024 + (kk & 3) * 2); };
   auto mstep = [](int kk) { return uint64_t(kk) * 128u; };
   int64_t kv_loads = 0;
-  bool ok = true, need_v = false;
+  bool ok = true;
   // S(it) goes to stage it&1, which the softmax of task it-2 must have read.
   auto issue_S = [&](int64_t it) -> bool {
     const int st = int(it & 1);
@@ -415,7 +500,6 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
   auto wait_kv = [&]() -> bool {
     if (!wait(bars.kv_full, uint32_t(kv_loads & 1))) return false;
     ++kv_loads;
-    need_v = true;
     return true;
   };
   int cur_kv = task_rec(tasks, 0, my_n).w;
@@ -429,10 +513,6 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
     if (!wait(bars.p_full[st], uint32_t((it >> 1) & 1))) break;
     // one O_part stage: the epilogue must have read O_part(it-1)
     if (it >= 1 && !wait(bars.o_free, uint32_t((it - 1) & 1))) break;
-    if (need_v) {
-      if (!wait(bars.v_ready, uint32_t((kv_loads - 1) & 1))) break;
-      need_v = false;
-    }
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
@@ -451,9 +531,6 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
   mbar_wait_drain(smem_u32(&bars.fin), 0);
 }
 
-// POOL_BF16: the O pool is bf16 (boxes of 64 columns) instead of fp32 (boxes
-// of 32 columns).
-template <bool POOL_BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_main(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -475,7 +552,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     skip_sh = plan_failed(p.header) ? 1 : 0;
     mbar_init(smem_u32(&bars.kv_full), 1);
     mbar_init(smem_u32(&bars.kv_empty), 1);
-    mbar_init(smem_u32(&bars.v_ready), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.q_full[i]), 1);
       mbar_init(smem_u32(&bars.q_empty[i]), 1);
@@ -498,9 +574,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
+  const int64_t ntasks = skip_sh ? 0 : p.header[kHdrFTasks];
   const int64_t my_n = cta_task_count(ntasks);
-  const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
+  const int4* tasks = reinterpret_cast<const int4*>(p.ftasks);
 
   if (warp == 0) {
     // ---------------- TMA producer (records and tokens prefetched one task ahead)
@@ -533,10 +609,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             break;
           const uint32_t b = smem_u32(&bars.kv_full);
           mbar_arrive_expect_tx(b, 2 * kTileBytes);
-          tma_load_3d(sbase + kSmK, &mapK, b, 0, tv.g, tv.key_start);
-          tma_load_3d(sbase + kSmK + 16384, &mapK, b, 64, tv.g, tv.key_start);
-          tma_load_3d(sbase + kSmV, &mapV, b, 0, tv.g, tv.key_start);
-          tma_load_3d(sbase + kSmV + 16384, &mapV, b, 64, tv.g, tv.key_start);
+          load_kv_tiles(sbase + kSmK, sbase + kSmV, &mapK, &mapV, b, tv.g, tv.key_start);
           ++kv_loads;
           prev_kv = tv.sub;
         }
@@ -544,14 +617,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (it >= 2 &&
             !mbar_wait(smem_u32(&bars.q_empty[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
           break;
-        const uint32_t b = smem_u32(&bars.q_full[st]);
-        mbar_arrive_expect_tx(b, kTileBytes);
-        const uint32_t dst = sbase + kSmQ + st * kTileBytes;
-#pragma unroll
-        for (int qi = 0; qi < kTaskQueries; ++qi) {
-          const int y = tok[qi] * kQHeads + tv.g * kHeadsPerGroup;
-          tma_load_2d(dst + qi * 2048, &mapQ, b, 0, y);
-          tma_load_2d(dst + 16384 + qi * 2048, &mapQ, b, 64, y);
+#ifdef MSA_TEST_STARVE
+        // test-only build: CTA 0 never loads its first Q tile, so the MMA
+        // issuer's bounded wait for it runs out
+        if (!(blockIdx.x == 0 && it == 0))
+#endif
+        {
+          const uint32_t b = smem_u32(&bars.q_full[st]);
+          mbar_arrive_expect_tx(b, kTileBytes);
+          load_q_tile(sbase + kSmQ + st * kTileBytes, &mapQ, b, tok, tv.g);
         }
         rec = rec1;
         rec1 = rec2;
@@ -567,31 +641,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, my_n, abort_flag);
-  } else if (warp == 14) {
-    // ---------------- V tile bf16 -> fp16 (scaled by an exact power of two)
-    if (my_n > 0) {
-      int prev_kv = -1;
-      int64_t kv_loads = 0;
-      for (int64_t it = 0; it < my_n; ++it) {
-        const int kv = task_rec(tasks, it, my_n).w;
-        if (kv == prev_kv) continue;
-        prev_kv = kv;
-        const float sc = v_scale_in(prm.vmax[kv]);
-        if (!mbar_wait_warp(smem_u32(&bars.kv_full), uint32_t(kv_loads & 1), abort_flag)) break;
-        ++kv_loads;
-        for (int i = lane; i < 2048; i += 32) {
-          const uint32_t a = sbase + kSmV + i * 16;
-          const uint4 x = ld_shared_v4(a);
-          st_shared_v4(a, pack_f16x2(bf16_lo(x.x) * sc, bf16_hi(x.x) * sc),
-                       pack_f16x2(bf16_lo(x.y) * sc, bf16_hi(x.y) * sc),
-                       pack_f16x2(bf16_lo(x.z) * sc, bf16_hi(x.z) * sc),
-                       pack_f16x2(bf16_lo(x.w) * sc, bf16_hi(x.w) * sc));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.v_ready));
-      }
-    }
   } else if (warp < 10) {
     // ---------------- softmax (warps 2-5: even tasks, 6-9: odd tasks)
     const int quad = warp & 3;
@@ -599,17 +648,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int row = quad * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
     const int qi = row >> 4, hh = row & 15;
+    // A row takes part when its query is real and not grouped (grouped
+    // queries are the group kernel's): jmax = last visible key, -1 if not.
+    auto row_jmax = [&](const TaskView& tv, int32_t tok) {
+      return (qi < tv.nq && !p.grouped[int64_t(tv.g) * p.T + tok])
+                 ? min(tok - tv.key_start, tv.key_len - 1)
+                 : -1;
+    };
     // Row data of this warpgroup's next task (it+2) is loaded while task it
     // runs, in two steps so no load result is consumed right after it is
-    // issued: the row's token at the top of task it, its shift M after the
-    // exponentials.
+    // issued: the row's token at the top of task it, its shift M and
+    // grouped flag after the exponentials.
     int4 rec1 = task_rec(tasks, par + 2, my_n);
     int jmax_c = -1;
     float m2_c = 0.f;
     if (par < my_n) {
       const TaskView tv = decode_task(task_rec(tasks, par, my_n));
       const int32_t tok = task_token(p.col, tv, qi);
-      jmax_c = qi < tv.nq ? min(tok - tv.key_start, tv.key_len - 1) : -1;
+      jmax_c = row_jmax(tv, tok);
       m2_c = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
     }
     for (int64_t it = par; it < my_n; it += 2) {
@@ -642,7 +698,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive(smem_u32(&bars.s_free[st]));
       {  // this warpgroup's next task
         const TaskView tn = decode_task(rec1);
-        jmax_c = qi < tn.nq ? min(ntok - tn.key_start, tn.key_len - 1) : -1;
+        jmax_c = row_jmax(tn, ntok);
         m2_c = prm.M2[int64_t(ntok) * kQHeads + tn.g * kHeadsPerGroup + hh];
       }
       // the epilogue of task it-2 has read this stage's row scalars
@@ -650,7 +706,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           !mbar_wait_warp(smem_u32(&bars.rs_free[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
         break;
       s_alpha[st][row] = jmax >= 0 ? fast_exp2(mxc - m2) : 0.f;
-      s_lrow[st][row] = lsum;
+      s_lrow[st][row] = jmax >= 0 ? lsum : -1.f;  // -1: the row takes no part
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[st]));
@@ -662,8 +718,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // two queries; the warp stages them in the 128-byte-swizzled box layout of
     // the pool's tensor map (conflict-free: the eight rows of a store phase
     // hit eight different 16-byte bank groups) and one lane adds them to the
-    // pool with four (fp32 pool) or two (bf16 pool) bulk tensor reductions
-    // per query.
+    // pool with four bulk tensor reductions per query.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
@@ -673,18 +728,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t swz = uint32_t(hh & 7);
     if (lane == 0 && my_n > 0) tma_prefetch_desc(&mapPool);
     int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
-    // the row's token and the block's V scale are loaded one task ahead
+    // the row's token is loaded one task ahead
     int32_t tok_c = my_n > 0 ? task_token(p.col, decode_task(rec), qi) : 0;
-    float vmax_c = my_n > 0 ? prm.vmax[rec.w] : 0.f;
     for (int64_t it = 0; it < my_n; ++it) {
       const int st = int(it & 1);
       const TaskView tv = decode_task(rec);
       const int4 rec2 = task_rec(tasks, it + 2, my_n);
       const int32_t tok = tok_c;
-      const float vmx = vmax_c;
       tok_c = task_token(p.col, decode_task(rec1), qi);  // rec1: a valid record
-      vmax_c = prm.vmax[rec1.w];
-      const bool valid = qi < tv.nq;
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;
       if (!mbar_wait_warp(smem_u32(&bars.o_full), uint32_t(it & 1), abort_flag)) break;
       // p_full(it) completed before o_full(it); waiting on it makes the
@@ -694,7 +745,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float alpha = s_alpha[st][row];
       const float lrow = s_lrow[st][row];
       mbar_arrive(smem_u32(&bars.rs_free[st]));
-      const float mul = alpha / v_scale_in(vmx);
+      const float mul = alpha * prm.vscale[tv.g];
+      // the warp's two queries take part? (rows 0 and 16 of the warp)
+      const bool take0 = __shfl_sync(0xffffffffu, lrow, 0) >= 0.f;
+      const bool take1 = __shfl_sync(0xffffffffu, lrow, 16) >= 0.f;
       // Boxes 0-1 (columns 0-63) and 2-3 (columns 64-127) of the warp's two
       // queries go out as two bulk groups, so the bulk engine reads one pair
       // while the warp stages the other: before a pair is overwritten, the
@@ -715,38 +769,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int qj = 2 * quad + j;
-          if (qj < tv.nq) {
+          if (j ? take1 : take0) {
             const int y = (j ? tok_hi : tok) * kQHeads + tv.g * kHeadsPerGroup;
 #pragma unroll
             for (int cq = cq0; cq < cq0 + 2; ++cq)
               tma_reduce_add_2d(&mapPool, sbase + kSmStage + uint32_t(qj) * 8192u + cq * 2048u,
                                 cq * 32, y);
-          }
-        }
-        bulk_commit();
-      };
-      // bf16 pool: box b holds columns [64b, 64b + 64) of the 16 rows; chunk u
-      // of a row (columns 64b + 8u ...) comes from a (u < 4) or b (u >= 4).
-      auto stage_box16 = [&](int b, const uint32_t (&a)[32], const uint32_t (&c)[32]) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t (&v)[32] = u < 4 ? a : c;
-          const int k = (u & 3) * 8;
-          st_shared_v4(stage_row + uint32_t(b) * 2048u + ((uint32_t(u) ^ swz) << 4),
-                       pack_bf16x2(__uint_as_float(v[k + 0]) * mul, __uint_as_float(v[k + 1]) * mul),
-                       pack_bf16x2(__uint_as_float(v[k + 2]) * mul, __uint_as_float(v[k + 3]) * mul),
-                       pack_bf16x2(__uint_as_float(v[k + 4]) * mul, __uint_as_float(v[k + 5]) * mul),
-                       pack_bf16x2(__uint_as_float(v[k + 6]) * mul, __uint_as_float(v[k + 7]) * mul));
-        }
-      };
-      auto issue_box16 = [&](int b) {  // box b of both queries
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int qj = 2 * quad + j;
-          if (qj < tv.nq) {
-            const int y = (j ? tok_hi : tok) * kQHeads + tv.g * kHeadsPerGroup;
-            tma_reduce_add_2d(&mapPool, sbase + kSmStage + uint32_t(qj) * 8192u + b * 2048u,
-                              b * 64, y);
           }
         }
         bulk_commit();
@@ -759,22 +787,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld_wait();
       reg_fence32(v0);
       reg_fence32(v1);
-      if constexpr (POOL_BF16) {
-        stage_box16(0, v0, v1);
-      } else {
-        stage_box(0, v0);
-        stage_box(1, v1);
-      }
+      stage_box(0, v0);
+      stage_box(1, v1);
       tmem_ld32(obase + 64, v0);
       tmem_ld32(obase + 96, v1);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (POOL_BF16)
-          issue_box16(0);
-        else
-          issue_pair(0);
-      }
+      if (lane == 0) issue_pair(0);
       __syncwarp();
       tmem_ld_wait();
       reg_fence32(v0);
@@ -783,21 +802,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive(smem_u32(&bars.o_free));  // O_part read: the next P.V may overwrite it
       if (lane == 0) bulk_wait_read1();  // previous task's boxes 2-3 read
       __syncwarp();
-      if constexpr (POOL_BF16) {
-        stage_box16(1, v0, v1);
-      } else {
-        stage_box(2, v0);
-        stage_box(3, v1);
-      }
+      stage_box(2, v0);
+      stage_box(3, v1);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (POOL_BF16)
-          issue_box16(1);
-        else
-          issue_pair(2);
-      }
-      if (valid) atomicAdd(prm.lsum + grow, alpha * lrow);
+      if (lane == 0) issue_pair(2);
+      if (lrow > 0.f) atomicAdd(prm.lsum + grow, alpha * lrow);
       rec = rec1;
       rec1 = rec2;
     }
@@ -811,14 +821,445 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ------------------------------------------------------------ fwd_group
+// One item: octet A (and octet B) of one index head, whose tokens all see the
+// same blocks.  The CTA walks those blocks: per block S_A = Q_A K^T and
+// S_B = Q_B K^T, P = exp(s - m_ref) as fp16 over S's own first 64 columns,
+// then O_A += P_A V and O_B += P_B V, O accumulating in TMEM across the
+// blocks.  m_ref is a row's reference maximum, set from the item's first
+// block and raised only when a later block's maximum passes it by more than
+// 15 octaves (so P < 2^16 stays in fp16); then O and the row sum are
+// rescaled in place.  After the last block the softmax warps write their
+// octet's O = acc / l and LSE: no pool, no finalize, no shift bound.
+//
+// P overwrites S, so the next S of an octet comes after its P.V; tensor-core
+// operations of one issuing thread run in issue order, so that needs no
+// wait.  The issue order S_A(j), P_B(j-1).V, S_B(j), P_A(j).V leaves each
+// octet's softmax two groups of MMAs (~1000 cycles) to run in.
+// Warp roles (320 threads):
+//   0     TMA producer: Q tiles of octets A and B (one buffer each: the next
+//         item's tile of an octet loads once the octet's last S of the
+//         current item is done), K and V per block (two stages each)
+//   1     MMA issuer (TMEM owner)
+//   2-5   softmax and epilogue of octet A (thread = tile row = TMEM lane)
+//   6-9   the same for octet B
+// TMEM: S_A [0,128) with P_A over [0,64), S_B [128,256) with P_B over
+// [128,192), O_A [256,384), O_B [384,512).
+// Items are placed by decreasing cost; CTA c takes items c, 2G-1-c, 2G+c, ...
+// (a snake over the G CTAs) so that the CTAs' totals balance.
+constexpr int kGrpThreads = 320;
+constexpr uint32_t kGsQ = 0, kGsK = 65536, kGsV = 131072;
+constexpr uint32_t kGrpSmem = kGsV + 2 * kTileBytes + 1024;
+constexpr uint32_t kGtO = 256;
+constexpr float kRaiseOctaves = 15.f;  // P = 2^(s - m_ref) < 2^16 fits fp16
+
+struct GrpBars {
+  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+      p_full[2], o_full[2], o_free[2], fin;
+};
+
+__device__ __forceinline__ int64_t item_index(int64_t i) {
+  const int64_t c = (i & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x);
+  return i * gridDim.x + c;
+}
+__device__ __forceinline__ int64_t item_count(int64_t n) {
+  const int64_t full = n / gridDim.x, rem = n % gridDim.x;
+  const int64_t c = (full & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x);
+  return full + (c < rem ? 1 : 0);
+}
+
+// P = 2^(s c2 - mref) of one tile row (TMEM columns [cs, cs + 128) of the
+// thread's lane) as fp16 pairs into pk (pair k = columns 2k, 2k+1), keys
+// after jmax masked when MASK; S is left intact.  Returns the sum of the
+// fp32 values; *tmax gets the row's maximum raw score.
+template <bool MASK>
+__device__ __forceinline__ float row_exp_regs(uint32_t cs, int jmax, float c2, float mref,
+                                              uint32_t (&pk)[64], float* tmax) {
+  const uint64_t cc = f2_pack(__float_as_uint(c2), __float_as_uint(c2));
+  const uint64_t nm = f2_pack(__float_as_uint(-mref), __float_as_uint(-mref));
+  uint64_t ls[2] = {0ull, 0ull};
+  float m0 = -INFINITY, m1 = -INFINITY;
+  auto expo = [&](const uint32_t (&r)[16], int l, int c) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      float x0 = __uint_as_float(r[j]), x1 = __uint_as_float(r[j + 1]);
+      const uint64_t x2 = f2_fma(f2_pack(r[j], r[j + 1]), cc, nm);
+      float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
+      if (MASK) {
+        p0 = j <= l ? p0 : 0.f;
+        p1 = j + 1 <= l ? p1 : 0.f;
+        x0 = j <= l ? x0 : -INFINITY;
+        x1 = j + 1 <= l ? x1 : -INFINITY;
+      }
+      if (j & 2) m1 = fmax3(m1, x0, x1); else m0 = fmax3(m0, x0, x1);
+      ls[(j >> 1) & 1] =
+          f2_add(ls[(j >> 1) & 1], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+      pk[8 * c + (j >> 1)] = pack_f16x2(p0, p1);
+    }
+  };
+  // chunk c+1 loads while chunk c is exponentiated
+  uint32_t r0[16], r1[16];
+  tmem_ld16(cs, r0);
+  tmem_ld_wait();
+  reg_fence16(r0);
+#pragma unroll
+  for (int c = 0; c < 8; c += 2) {
+    tmem_ld16(cs + 16 * c + 16, r1);
+    expo(r0, jmax - 16 * c, c);
+    tmem_ld_wait();
+    reg_fence16(r1);
+    if (c < 6) tmem_ld16(cs + 16 * c + 32, r0);
+    expo(r1, jmax - 16 * c - 16, c + 1);
+    if (c < 6) {
+      tmem_ld_wait();
+      reg_fence16(r0);
+    }
+  }
+  *tmax = fmaxf(m0, m1);
+  const uint64_t s2 = f2_add(ls[0], ls[1]);
+  return f2_lo(s2) + f2_hi(s2);
+}
+
+// MMA issuer of k_fwd_group (one thread).
+__device__ __noinline__ void grp_mma_role(GrpBars& bars, uint32_t tmem, uint32_t sbase,
+                                          const int32_t* items, int64_t my_n,
+                                          volatile int* abort_flag) {
+  constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T  (bf16)
+  constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V    (fp16, P in TMEM)
+  auto wait = [&](uint64_t& bar, uint32_t ph) {
+    return mbar_wait(smem_u32(&bar), ph, abort_flag);
+  };
+  const uint64_t kQ0 = sdesc_sw128(sbase + kGsQ, 16u, 1024u);
+  const uint64_t kK0 = sdesc_sw128(sbase + kGsK, 16u, 1024u);
+  const uint64_t mV0 = sdesc_sw128(sbase + kGsV, 16384u, 1024u);
+  constexpr uint64_t kStage = kTileBytes >> 4;
+  auto kstep = [](int kk) { return uint64_t((kk >> 2) * 1024 + (kk & 3) * 2); };
+  auto mstep = [](int kk) { return uint64_t(kk) * 128u; };
+  int64_t nblk = 0;          // blocks walked (K / V stage phases)
+  int64_t nx[2] = {0, 0};    // blocks per octet slot (s_full / p_full phases)
+  int64_t ix[2] = {0, 0};    // items per octet slot (o_full / o_free phases)
+  int64_t qu[2] = {0, 0};    // uses of the two Q buffers
+  auto issue_S = [&](int x, int stg) {
+    const uint64_t bq = kQ0 + uint64_t(x) * kStage;
+    const uint64_t bk = kK0 + uint64_t(stg) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(tmem + 128 * x, bq + kstep(kk), bk + kstep(kk), idS, kk > 0);
+    umma_commit(smem_u32(&bars.s_full[x]));
+  };
+  // O_x += P_x . V of the block in V stage stg (first block: O_x = ...)
+  auto issue_PV = [&](int x, int stg, bool first) -> bool {
+    if (!wait(bars.p_full[x], uint32_t(nx[x] & 1))) return false;
+    if (first && ix[x] > 0 && !wait(bars.o_free[x], uint32_t((ix[x] - 1) & 1))) return false;
+    tc_fence_after();
+    const uint64_t bv = mV0 + uint64_t(stg) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ts(tmem + kGtO + 128 * x, tmem + 128 * x + kk * 8, bv + mstep(kk), idPV,
+              (!first || kk > 0) ? 1u : 0u);
+    ++nx[x];
+    return true;
+  };
+  // the previous block's P_B . V, issued after the next S_A
+  bool pend = false, pend_first = false, pend_last = false;
+  int pend_stg = 0;
+  auto flush_B = [&]() -> bool {
+    if (!pend) return true;
+    if (!issue_PV(1, pend_stg, pend_first)) return false;
+    umma_commit(smem_u32(&bars.v_empty[pend_stg]));
+    if (pend_last) {
+      umma_commit(smem_u32(&bars.o_full[1]));
+      ++ix[1];
+    }
+    pend = false;
+    return true;
+  };
+  bool ok = true;
+  for (int64_t i = 0; ok && i < my_n; ++i) {
+    const ItemView iv = decode_item(items + item_index(i) * kItemWords);
+    const bool hasB = iv.tokB >= 0;
+    for (int j = 0; j < iv.nsel; ++j) {
+      const int stg = int(nblk & 1);
+      const uint32_t ph = uint32_t((nblk >> 1) & 1);
+      const bool last = j + 1 == iv.nsel;
+      if (!wait(bars.k_full[stg], ph)) { ok = false; break; }
+      if (j == 0 && !wait(bars.q_full[0], uint32_t(qu[0] & 1))) { ok = false; break; }
+      tc_fence_after();
+      issue_S(0, stg);
+      if (last) {
+        umma_commit(smem_u32(&bars.q_empty[0]));
+        ++qu[0];
+      }
+      if (!flush_B()) { ok = false; break; }
+      if (hasB) {
+        if (j == 0 && !wait(bars.q_full[1], uint32_t(qu[1] & 1))) { ok = false; break; }
+        tc_fence_after();
+        issue_S(1, stg);
+        if (last) {
+          umma_commit(smem_u32(&bars.q_empty[1]));
+          ++qu[1];
+        }
+      }
+      umma_commit(smem_u32(&bars.k_empty[stg]));  // K of this block: both S issued
+      if (!wait(bars.v_full[stg], ph)) { ok = false; break; }
+      if (!issue_PV(0, stg, j == 0)) { ok = false; break; }
+      if (last) {
+        umma_commit(smem_u32(&bars.o_full[0]));
+        ++ix[0];
+      }
+      if (hasB) {
+        pend = true;
+        pend_stg = stg;
+        pend_first = j == 0;
+        pend_last = last;
+      } else {
+        umma_commit(smem_u32(&bars.v_empty[stg]));
+      }
+      ++nblk;
+    }
+  }
+  if (ok) flush_B();
+  umma_commit(smem_u32(&bars.fin));
+  mbar_wait_drain(smem_u32(&bars.fin), 0);
+}
+
+__global__ void __launch_bounds__(kGrpThreads, 1)
+    k_fwd_group(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
+                const __grid_constant__ CUtensorMap mapK,
+                const __grid_constant__ CUtensorMap mapV) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ GrpBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, skip_sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const msa_plan& p = prm.plan;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    skip_sh = plan_failed(p.header) ? 1 : 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.q_full[i]), 1);
+      mbar_init(smem_u32(&bars.q_empty[i]), 1);
+      mbar_init(smem_u32(&bars.k_full[i]), 1);
+      mbar_init(smem_u32(&bars.k_empty[i]), 1);
+      mbar_init(smem_u32(&bars.v_full[i]), 1);
+      mbar_init(smem_u32(&bars.v_empty[i]), 1);
+      mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_full[i]), 128);
+      mbar_init(smem_u32(&bars.o_full[i]), 1);
+      mbar_init(smem_u32(&bars.o_free[i]), 128);
+    }
+    mbar_init(smem_u32(&bars.fin), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int64_t nitems = skip_sh ? 0 : p.header[kHdrItems];
+  const int64_t my_n = item_count(nitems);
+  const int32_t* items = p.items;
+  const DocInfo* dinfo = reinterpret_cast<const DocInfo*>(p.doc_info);
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0 && my_n > 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      int64_t nblk = 0, qu[2] = {0, 0};
+      bool ok = true;
+      auto load_q = [&](int buf, int32_t tok0, int nq, int g) -> bool {
+        if (qu[buf] > 0 &&
+            !mbar_wait(smem_u32(&bars.q_empty[buf]), uint32_t((qu[buf] - 1) & 1), abort_flag))
+          return false;
+#ifdef MSA_TEST_STARVE
+        // test-only build: CTA 0 never loads its first Q tile, so the waits
+        // for it run out
+        if (blockIdx.x == 0 && buf == 0 && qu[0] == 0) {
+          ++qu[buf];
+          return true;
+        }
+#endif
+        int32_t tok[kTaskQueries];
+#pragma unroll
+        for (int qi = 0; qi < kTaskQueries; ++qi) tok[qi] = tok0 + (qi < nq ? qi : nq - 1);
+        const uint32_t b = smem_u32(&bars.q_full[buf]);
+        mbar_arrive_expect_tx(b, kTileBytes);
+        load_q_tile(sbase + kGsQ + buf * kTileBytes, &mapQ, b, tok, g);
+        ++qu[buf];
+        return true;
+      };
+      // K and V of one block into stage nblk & 1 of their rings
+      auto load_kv = [&](int g, int32_t key_start) -> bool {
+        const int stg = int(nblk & 1);
+        const uint32_t ph = uint32_t(((nblk >> 1) - 1) & 1);
+        if (nblk >= 2 && !mbar_wait(smem_u32(&bars.k_empty[stg]), ph, abort_flag)) return false;
+        uint32_t b = smem_u32(&bars.k_full[stg]);
+        mbar_arrive_expect_tx(b, kTileBytes);
+        tma_load_3d(sbase + kGsK + stg * kTileBytes, &mapK, b, 0, g, key_start);
+        tma_load_3d(sbase + kGsK + stg * kTileBytes + 16384, &mapK, b, 64, g, key_start);
+        if (nblk >= 2 && !mbar_wait(smem_u32(&bars.v_empty[stg]), ph, abort_flag)) return false;
+        b = smem_u32(&bars.v_full[stg]);
+        mbar_arrive_expect_tx(b, kTileBytes);
+        tma_load_3d(sbase + kGsV + stg * kTileBytes, &mapV, b, 0, g, key_start);
+        tma_load_3d(sbase + kGsV + stg * kTileBytes + 16384, &mapV, b, 64, g, key_start);
+        ++nblk;
+        return true;
+      };
+      for (int64_t i = 0; ok && i < my_n; ++i) {
+        const int32_t* it = items + item_index(i) * kItemWords;
+        const ItemView iv = decode_item(it);
+        const int32_t dstart = dinfo[iv.doc].start;
+        // A's tile, K/V of the first block, B's tile, the other blocks
+        ok = load_q(0, iv.tokA, iv.nqA, iv.g);
+        for (int j = 0; ok && j < iv.nsel; ++j) {
+          ok = load_kv(iv.g, dstart + it[4 + j] * kBlock);
+          if (ok && j == 0 && iv.tokB >= 0) ok = load_q(1, iv.tokB, iv.nqB, iv.g);
+        }
+      }
+      if (*abort_flag) {  // let armed copies land before the CTA exits
+        for (int64_t j = (nblk >= 2 ? nblk - 2 : 0); j < nblk; ++j) {
+          mbar_wait_drain(smem_u32(&bars.k_full[j & 1]), uint32_t((j >> 1) & 1));
+          mbar_wait_drain(smem_u32(&bars.v_full[j & 1]), uint32_t((j >> 1) & 1));
+        }
+        for (int b = 0; b < 2; ++b)
+          if (qu[b] > 0) mbar_wait_drain(smem_u32(&bars.q_full[b]), uint32_t((qu[b] - 1) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0 && my_n > 0) grp_mma_role(bars, tmem, sbase, items, my_n, abort_flag);
+  } else {
+    // ---------------- softmax + epilogue of octet x (warps 2-5: A, 6-9: B)
+    const int x = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // tile row = TMEM lane
+    const uint32_t lane_base = uint32_t(quad * 32) << 16;
+    const int qi = row >> 4, hh = row & 15;
+    const uint32_t cs = tmem + lane_base + 128 * x;
+    const uint32_t co = tmem + lane_base + kGtO + 128 * x;
+    int64_t nx = 0, ix = 0;
+    for (int64_t i = 0; i < my_n; ++i) {
+      const int32_t* it = items + item_index(i) * kItemWords;
+      const ItemView iv = decode_item(it);
+      if (x == 1 && iv.tokB < 0) continue;
+      const int32_t tok0 = x ? iv.tokB : iv.tokA;
+      const int nq = x ? iv.nqB : iv.nqA;
+      const int32_t tok = tok0 + (qi < nq ? qi : nq - 1);
+      const int32_t dstart = dinfo[iv.doc].start;
+      float mref = -INFINITY, lsum = 0.f;
+      bool ok = true;
+      for (int j = 0; j < iv.nsel; ++j) {
+        const int32_t key_start = dstart + it[4 + j] * kBlock;
+        const int jmax = qi < nq ? min(tok - key_start, kBlock - 1) : -1;
+        // S_x(j) complete: so is P_x(j-1) . V, which was issued before it
+        if (!mbar_wait_warp(smem_u32(&bars.s_full[x]), uint32_t(nx & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool full = __all_sync(0xffffffffu, jmax == kBlock - 1);
+        if (j == 0) {  // the item's first block sets the reference
+          const float mx = full ? tile_row_max<false>(cs, jmax) : tile_row_max<true>(cs, jmax);
+          mref = jmax >= 0 ? mx * prm.c2 : -INFINITY;
+        }
+        uint32_t pk[64];
+        float tmax;
+        float ls = full ? row_exp_regs<false>(cs, jmax, prm.c2, mref, pk, &tmax)
+                        : row_exp_regs<true>(cs, jmax, prm.c2, mref, pk, &tmax);
+        const float mxc = tmax * prm.c2;
+        const bool raise = j > 0 && jmax >= 0 && mxc > mref + kRaiseOctaves;
+        if (__any_sync(0xffffffffu, raise)) {
+          // rescale O (complete up to block j-1) and the row sum by
+          // 2^(mref - mxc), then redo the exponentials (S is still intact)
+          const float f = raise ? fast_exp2(mref - mxc) : 1.f;
+          lsum *= f;
+          if (raise) mref = mxc;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(co + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32_nc(co + 32 * c, o);
+          }
+          ls = full ? row_exp_regs<false>(cs, jmax, prm.c2, mref, pk, &tmax)
+                    : row_exp_regs<true>(cs, jmax, prm.c2, mref, pk, &tmax);
+        }
+        lsum += ls;
+        // P over the first 64 columns of S (all of S has been read)
+        tmem_st32_nc(cs, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32_nc(cs + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.p_full[x]));
+        ++nx;
+      }
+      if (!ok) break;
+      // ---- epilogue: O = acc / l, LSE
+      if (!mbar_wait_warp(smem_u32(&bars.o_full[x]), uint32_t(ix & 1), abort_flag)) break;
+      ++ix;
+      tc_fence_after();
+      uint32_t o[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(co + 32 * c, o[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(o[c]);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.o_free[x]));  // the next item's P.V may overwrite O_x
+      if (qi < nq) {
+        const int64_t grow = int64_t(tok) * kQHeads + iv.g * kHeadsPerGroup + hh;
+        if (!(lsum > 0.f) || !isfinite(lsum)) {
+          const int32_t k = atomicAdd(prm.list, 1);  // the fallback writes this row
+          prm.list[1 + k] = int32_t(grow);
+        } else {
+          const float inv = prm.vscale[iv.g] / lsum;
+          uint4* dst = reinterpret_cast<uint4*>(prm.O + grow * kHeadDim);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t* v = &o[c][8 * u];
+              dst[4 * c + u] = make_uint4(
+                  pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                  pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                  pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                  pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+            }
+          prm.lse[grow] = (mref + __log2f(lsum)) * kLn2;
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown
+  if (threadIdx.x == 0 && abort_sh) raise_status(p.header, MSA_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 // ------------------------------------------------------------ fwd_finalize
-// O = pool / sum -> bf16 and LSE = (M + log2 sum) ln 2.  Each warp finishes
-// eight rows per step (16 lanes x 8 elements per row), all loads issued
-// before any use.  Rows whose sum underflowed are listed for the fallback.
+// Pooled rows: O = pool / sum -> bf16 and LSE = (M + log2 sum) ln 2.  Each
+// warp finishes eight rows per step (16 lanes x 8 elements per row; the
+// eight rows are heads of one token and index head), all loads issued before
+// any use.  Grouped rows were written by the group kernel.  Rows whose sum
+// underflowed are listed for the fallback.
 constexpr int kFinRowsPerWarp = 8;
-template <bool POOL_BF16>
 __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M2,
-                                                      const float* lsum, const void* pool,
+                                                      const float* lsum, const float* pool,
                                                       __nv_bfloat16* O, float* lse,
                                                       int32_t* list) {
   if (plan_failed(p.header)) return;
@@ -827,34 +1268,23 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
   const int64_t nwarps = int64_t(gridDim.x) * blockDim.x / 32;
   for (int64_t r0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32 * kFinRowsPerWarp;
        r0 < rows; r0 += nwarps * kFinRowsPerWarp) {
+    const int64_t t = r0 / kQHeads;
+    const int g = int(r0 % kQHeads) / kHeadsPerGroup;
+    if (p.grouped[int64_t(g) * p.T + t]) continue;
     float4 a[4], b[4];
-    uint4 h[4];  // bf16 pool: the 8 elements, widened after all loads
     float m2[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t row = r0 + 2 * i + (lane >> 4);
-      if (row < rows) {
-        if constexpr (POOL_BF16) {
-          h[i] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(pool) +
-                                                row * kHeadDim)[sub];
-        } else {
-          const float4* src =
-              reinterpret_cast<const float4*>(static_cast<const float*>(pool) + row * kHeadDim) +
-              2 * sub;
-          a[i] = src[0];
-          b[i] = src[1];
-        }
-        m2[i] = M2[row];
-        l[i] = lsum[row];
-      } else {
-        m2[i] = -INFINITY;
-        l[i] = 0.f;
-      }
+      const float4* src = reinterpret_cast<const float4*>(pool + row * kHeadDim) + 2 * sub;
+      a[i] = src[0];
+      b[i] = src[1];
+      m2[i] = M2[row];
+      l[i] = lsum[row];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int64_t row = r0 + 2 * i + (lane >> 4);
-      if (row >= rows) continue;
       uint4 out = make_uint4(0u, 0u, 0u, 0u);
       float L = -INFINITY;
       if (m2[i] != -INFINITY) {
@@ -866,10 +1296,6 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
           continue;  // the fallback kernel writes this row
         }
         const float inv = 1.f / l[i];
-        if constexpr (POOL_BF16) {
-          a[i] = make_float4(bf16_lo(h[i].x), bf16_hi(h[i].x), bf16_lo(h[i].y), bf16_hi(h[i].y));
-          b[i] = make_float4(bf16_lo(h[i].z), bf16_hi(h[i].z), bf16_lo(h[i].w), bf16_hi(h[i].w));
-        }
         out = make_uint4(pack_bf16x2(a[i].x * inv, a[i].y * inv), pack_bf16x2(a[i].z * inv, a[i].w * inv),
                          pack_bf16x2(b[i].x * inv, b[i].y * inv), pack_bf16x2(b[i].z * inv, b[i].w * inv));
         L = (m2[i] + __log2f(l[i])) * kLn2;
@@ -946,7 +1372,6 @@ __global__ void __launch_bounds__(256) k_fwd_fallback(msa_plan p, const __nv_bfl
 CUresult make_map_rows(CUtensorMap* m, const void* base, int64_t rows);      // msa_api.cu
 CUresult make_map_kv(CUtensorMap* m, const void* base, int64_t T);           // msa_api.cu
 CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows);    // msa_api.cu
-CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows);    // msa_api.cu
 int device_sm_count();                                                       // msa_api.cu
 
 size_t forward_workspace_bytes(const msa_plan& p) { return fwd_layout(p).total; }
@@ -958,17 +1383,18 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   float* M2 = reinterpret_cast<float*>(w + L.off_m);
   float* lsum = reinterpret_cast<float*>(w + L.off_l);
   float* vmax = reinterpret_cast<float*>(w + L.off_vmax);
-  uint8_t* pool = w + L.off_pool;
-  const bool pool16 = p.o_accum == MSA_O_ACCUM_BF16;
+  float* pool = reinterpret_cast<float*>(w + L.off_pool);
   float* kmax = reinterpret_cast<float*>(w + L.off_kmax);
   int32_t* list = reinterpret_cast<int32_t*>(w + L.off_list);
+  uint4* v16 = reinterpret_cast<uint4*>(w + L.off_v16);
+  float* vscale = reinterpret_cast<float*>(w + L.off_vscale);
   const float c2 = scale * kLog2e;
 
+  // V tiles are read from the fp16 copy (same element size, same map shape)
   CUtensorMap mQ, mK, mV, mPool;
   if (make_map_rows(&mQ, q, p.T * kQHeads) != CUDA_SUCCESS ||
-      make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v, p.T) != CUDA_SUCCESS ||
-      (pool16 ? make_map_pool16(&mPool, pool, p.T * kQHeads)
-              : make_map_pool32(&mPool, pool, p.T * kQHeads)) != CUDA_SUCCESS)
+      make_map_kv(&mK, k, p.T) != CUDA_SUCCESS || make_map_kv(&mV, v16, p.T) != CUDA_SUCCESS ||
+      make_map_pool32(&mPool, pool, p.T * kQHeads) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   cudaError_t e;
@@ -977,35 +1403,36 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
                                                 static_cast<const __nv_bfloat16*>(v), kmax, vmax,
                                                 list);
   launch_end("fwd_kmax", s);
+  launch_begin("fwd_v16", s);
+  k_fwd_v16<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(
+      p, static_cast<const __nv_bfloat16*>(v), vmax, v16, vscale);
+  launch_end("fwd_v16", s);
   const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
   k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool,
-      int(pool_elem_bytes(p)));
+      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
   launch_end("fwd_rows", s);
 
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[pool16]) {
-    e = cudaFuncSetAttribute(pool16 ? k_fwd_main<true> : k_fwd_main<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(k_fwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
     if (e != cudaSuccess) return e;
-    attr_set[pool16] = true;
+    e = cudaFuncSetAttribute(k_fwd_group, cudaFuncAttributeMaxDynamicSharedMemorySize, kGrpSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
-  FwdParams prm{p, M2, vmax, pool, lsum, c2};
+  FwdParams prm{p,    M2,   kmax, vmax, pool, lsum, list, static_cast<__nv_bfloat16*>(o),
+                lse,  vscale, c2};
   const unsigned grid = unsigned(device_sm_count());
+  launch_begin("fwd_group", s);
+  k_fwd_group<<<grid, kGrpThreads, kGrpSmem, s>>>(prm, mQ, mK, mV);
+  launch_end("fwd_group", s);
   launch_begin("fwd_main", s);
-  if (pool16)
-    k_fwd_main<true><<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
-  else
-    k_fwd_main<false><<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
+  k_fwd_main<<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
   launch_end("fwd_main", s);
   launch_begin("fwd_finalize", s);
-  if (pool16)
-    k_fwd_finalize<true><<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool,
-                                                   static_cast<__nv_bfloat16*>(o), lse, list);
-  else
-    k_fwd_finalize<false><<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool,
-                                                    static_cast<__nv_bfloat16*>(o), lse, list);
+  k_fwd_finalize<<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o),
+                                           lse, list);
   launch_end("fwd_finalize", s);
   launch_begin("fwd_fallback", s);
   k_fwd_fallback<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(

@@ -30,8 +30,13 @@ enum HeaderSlot {
   kHdrTasks = 4,    // tasks
   kHdrPairs = 5,    // attended (query, head, key) triples
   kHdrTriPerG = 6,  // count entries per index head
-  kHdrWords = 16
+  kHdrItems = 7,    // octet-group items of the forward
+  kHdrFTasks = 8,   // tasks of the forward's pooled task list
+  kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..32)
+  kHdrCostFill = 56,  // placement counters of the items, per cost
+  kHdrWords = 96
 };
+constexpr int kMaxItemCost = 2 * 16;  // an item: at most 2 octets x 16 blocks
 
 __device__ __forceinline__ void raise_status(int64_t* header, msa_status s) {
   atomicOr(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
@@ -70,6 +75,29 @@ __device__ __forceinline__ TaskView decode_task(int4 t) {
   return v;
 }
 
+// Octet-group item of the forward (int32 [kItemWords]): the tiles of one or
+// two aligned octets (8 consecutive tokens of a document, positions 8k ..
+// 8k+7, fewer at its end) whose tokens all see the same selected blocks.
+//   [0] first token of octet A, [1] first token of octet B (-1: none),
+//   [2] queries of A | queries of B << 4 | index head << 8 | blocks << 12,
+//   [3] document index, [4 .. 20) the blocks (document-local, ascending, -1).
+constexpr int kItemWords = 20;
+struct ItemView {
+  int32_t tokA, tokB, nqA, nqB, g, nsel, doc;
+};
+__device__ __forceinline__ ItemView decode_item(const int32_t* it) {
+  const int4 h = *reinterpret_cast<const int4*>(it);
+  ItemView v;
+  v.tokA = h.x;
+  v.tokB = h.y;
+  v.nqA = h.z & 0xF;
+  v.nqB = (h.z >> 4) & 0xF;
+  v.g = (h.z >> 8) & 0x3;
+  v.nsel = (h.z >> 12) & 0x1F;
+  v.doc = h.w;
+  return v;
+}
+
 // Index of count entry (g, doc, key block v, query block qb), v <= qb < n, in
 // the order (g, doc, super-block of qb, v, qb): tasks emitted in this order
 // walk one super-block of queries at a time.  Zs = super-block length in
@@ -90,9 +118,9 @@ __host__ __device__ __forceinline__ int64_t tri_local(int64_t n, int64_t Zs, int
 
 // Workspace layout of a plan, shared by the size query and msa_build_plan.
 struct PlanLayout {
-  int64_t nb_cap, tri_cap, nnz_cap, task_cap, scan_tmp_len;
+  int64_t nb_cap, tri_cap, nnz_cap, task_cap, item_cap, scan_tmp_len;
   size_t off_header, off_doc_info, off_doc_tri, off_cnt, off_off, off_col, off_tcnt, off_toff,
-      off_tasks, off_scan, total;
+      off_tasks, off_scan, off_grouped, off_items, off_fflag, off_fpos, off_ftasks, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -107,7 +135,9 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
   L.tri_cap = 4 * ((D - 1) + x * (x + 1) / 2);
   L.nnz_cap = int64_t(kKVHeads) * kTopK * T;
   L.task_cap = L.nnz_cap / kTaskQueries + L.tri_cap;
-  L.scan_tmp_len = (L.tri_cap + 4095) / 4096 + 64;
+  // a document of n tokens has ceil(n / 8) <= n / 8 + 1 octets
+  L.item_cap = int64_t(kKVHeads) * (T / 8 + D);
+  L.scan_tmp_len = ((L.tri_cap > L.task_cap ? L.tri_cap : L.task_cap) + 4095) / 4096 + 64;
   size_t o = 0;
   L.off_header = o;   o = align_up(o + sizeof(int64_t) * kHdrWords, 256);
   L.off_doc_info = o; o = align_up(o + sizeof(DocInfo) * D, 256);
@@ -119,6 +149,11 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
   L.off_toff = o;     o = align_up(o + sizeof(int32_t) * L.tri_cap, 256);
   L.off_tasks = o;    o = align_up(o + sizeof(int4) * L.task_cap, 256);
   L.off_scan = o;     o = align_up(o + sizeof(int32_t) * L.scan_tmp_len, 256);
+  L.off_grouped = o;  o = align_up(o + sizeof(uint8_t) * kKVHeads * T, 256);
+  L.off_items = o;    o = align_up(o + sizeof(int32_t) * kItemWords * L.item_cap, 256);
+  L.off_fflag = o;    o = align_up(o + sizeof(int32_t) * L.task_cap, 256);
+  L.off_fpos = o;     o = align_up(o + sizeof(int32_t) * L.task_cap, 256);
+  L.off_ftasks = o;   o = align_up(o + sizeof(int4) * L.task_cap, 256);
   L.total = o;
   return L;
 }

@@ -178,20 +178,6 @@ CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// The same pool in bf16: box = 16 rows x 64 columns (128 bytes), 128-byte
-// swizzle.
-CUresult make_map_pool16(CUtensorMap* m, const void* base, int64_t rows) {
-  auto fn = encode_fn();
-  if (!fn) return CUDA_ERROR_NOT_FOUND;
-  cuuint64_t gd[2] = {cuuint64_t(kHeadDim), cuuint64_t(rows)};
-  cuuint64_t gs[1] = {cuuint64_t(kHeadDim * 2)};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
 }  // namespace msa
 
 using namespace msa;
@@ -266,13 +252,21 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   p.tasks = reinterpret_cast<int32_t*>(w + L.off_tasks);
   p.scan_tmp = reinterpret_cast<int32_t*>(w + L.off_scan);
   p.scan_tmp_len = L.scan_tmp_len;
+  p.item_cap = L.item_cap;
+  p.grouped = reinterpret_cast<uint8_t*>(w + L.off_grouped);
+  p.items = reinterpret_cast<int32_t*>(w + L.off_items);
+  p.fflag = reinterpret_cast<int32_t*>(w + L.off_fflag);
+  p.fpos = reinterpret_cast<int32_t*>(w + L.off_fpos);
+  p.ftasks = reinterpret_cast<int32_t*>(w + L.off_ftasks);
   if (launch_plan(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MSA_ERR_CUDA;
   *out = p;
   return MSA_OK;
 }
 
 static msa_status check_plan(const msa_plan* plan) {
-  if (!plan || plan->T < 1 || !plan->header || !plan->tasks) return MSA_ERR_INVALID_ARG;
+  if (!plan || plan->T < 1 || !plan->header || !plan->tasks || !plan->ftasks || !plan->items ||
+      !plan->grouped)
+    return MSA_ERR_INVALID_ARG;
   return MSA_OK;
 }
 
@@ -352,12 +346,14 @@ msa_status msa_plan_counts(const msa_plan* plan, msa_stream_t stream, int64_t* c
   counts[2] = h[kHdrTasks];
   counts[3] = h[kHdrPairs];
   counts[4] = h[kHdrTri];
+  counts[5] = h[kHdrItems];
+  counts[6] = h[kHdrFTasks];
   return MSA_OK;
 }
 
 msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* col,
                            int64_t col_capacity, int32_t* tasks, int64_t task_capacity) {
-  int64_t c[5];
+  int64_t c[7];
   msa_status st = msa_plan_counts(plan, stream, c);
   if (st != MSA_OK) return st;
   if ((col && col_capacity < c[1]) || (tasks && task_capacity < c[2])) return MSA_ERR_INVALID_ARG;
@@ -366,6 +362,30 @@ msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* c
     return MSA_ERR_CUDA;
   if (tasks && c[2] > 0 &&
       cudaMemcpy(tasks, plan->tasks, sizeof(int32_t) * 4 * c[2], cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
+msa_status msa_plan_export_groups(const msa_plan* plan, msa_stream_t stream, uint8_t* grouped,
+                                  int64_t grouped_capacity, int32_t* items,
+                                  int64_t item_capacity, int32_t* ftasks,
+                                  int64_t ftask_capacity) {
+  int64_t c[7];
+  msa_status st = msa_plan_counts(plan, stream, c);
+  if (st != MSA_OK) return st;
+  if ((grouped && grouped_capacity < plan->T) || (items && item_capacity < c[5]) ||
+      (ftasks && ftask_capacity < c[6]))
+    return MSA_ERR_INVALID_ARG;
+  if (grouped && cudaMemcpy(grouped, plan->grouped, size_t(kKVHeads) * plan->T,
+                            cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (items && c[5] > 0 &&
+      cudaMemcpy(items, plan->items, sizeof(int32_t) * kItemWords * c[5],
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (ftasks && c[6] > 0 &&
+      cudaMemcpy(ftasks, plan->ftasks, sizeof(int32_t) * 4 * c[6], cudaMemcpyDeviceToHost) !=
           cudaSuccess)
     return MSA_ERR_CUDA;
   return MSA_OK;

@@ -9,6 +9,15 @@
 // is launched with capacity-bounded grids; exact counts are read from the
 // plan header.
 //
+// Octet groups.  The same CTA sees, per key block, which of its 128 queries
+// selected it, so it also finds the block's aligned octets (8 queries) whose
+// queries all see the same non-empty block set: their tiles can accumulate
+// block after block in one place (the forward's group kernel), and the
+// forward's pooled task list leaves out the tasks made only of such queries.
+// Two such octets 2i, 2i+1 with the same set form one item.  Items are placed
+// by decreasing cost (blocks x octets) so that a round-robin walk over them
+// balances.
+//
 // Count entries.  For index head g, document d (n blocks), key block v and
 // query block qb >= v, entry (g, d, v, qb) counts the queries of block qb that
 // selected v.  Entries are ordered (g, d, super-block of qb, v, qb) - see
@@ -120,6 +129,8 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
   __shared__ uint32_t bm[kChunkV][4];
   __shared__ int s_doc, s_skip;
   __shared__ unsigned long long s_pairs;
+  __shared__ int s_nsel[16];        // per octet: blocks selected by any of its queries
+  __shared__ uint32_t s_bad, s_pdiff;  // octets not uniform; pairs with different sets
   int64_t* hdr = p.header;
   const int64_t NB = hdr[kHdrNB];
   const int g = int(blockIdx.x / p.nb_cap);
@@ -136,7 +147,10 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
     }
     s_doc = lo;
     s_pairs = 0;
+    s_bad = 0u;
+    s_pdiff = 0u;
   }
+  if (threadIdx.x < 16) s_nsel[threadIdx.x] = 0;
   __syncthreads();
   if (s_skip) return;
   const int d = s_doc;
@@ -177,6 +191,15 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
   const int64_t lo_q = (qb / Zs) * Zs;       // first query block of this super-block
   const int64_t hi_q = lo_q + Zs < n ? lo_q + Zs : n;
   int64_t pairs = 0;
+  // octet scan: thread r looks at octet r % 16 for every eighth key block
+  const int oct = r & 15;
+  auto octet_rows = [&](int o) -> int {  // valid queries of octet o
+    const int64_t rem = int64_t(di.len) - (qb * kBlock + 8 * o);
+    return rem <= 0 ? 0 : (rem >= 8 ? 8 : int(rem));
+  };
+  const uint32_t oct_mask = (1u << octet_rows(oct)) - 1u;
+  int my_nsel = 0;
+  bool my_bad = false, my_pdiff = false;
 
   for (int64_t c0 = 0; c0 <= qb; c0 += kChunkV) {
     const int64_t cend = (c0 + kChunkV - 1 < qb) ? c0 + kChunkV - 1 : qb;
@@ -189,6 +212,17 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
         if (sl[i] >= c0 && sl[i] <= cend) atomicOr(&bm[sl[i] - c0][r >> 5], 1u << (r & 31));
     }
     __syncthreads();
+    if (PASS != kPassEmit) {
+      for (int v = r >> 4; v < span; v += 8) {
+        const uint32_t b0 = (bm[v][oct >> 2] >> ((oct & 3) * 8)) & 0xFFu;
+        my_nsel += b0 != 0u;
+        my_bad |= b0 != 0u && b0 != oct_mask;
+        if (!(oct & 1)) {
+          const uint32_t b1 = (bm[v][(oct + 1) >> 2] >> (((oct + 1) & 3) * 8)) & 0xFFu;
+          my_pdiff |= (b0 != 0u) != (b1 != 0u);
+        }
+      }
+    }
     if (PASS == kPassCount) {
       for (int64_t v = c0 + threadIdx.x; v <= cend; v += blockDim.x) {
         const uint32_t* b = bm[v - c0];
@@ -244,10 +278,66 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
           task.z = key_len | (nq << 8) | (g << 12);
           task.w = int32_t(int64_t(g) * p.nb_cap + di.blk_base + v);
           reinterpret_cast<int4*>(p.tasks)[p.toff[e] + i] = task;
+          // the forward's pooled list keeps tasks with an ungrouped query
+          int keep = 0;
+          for (int k = 0; k < nq; ++k)
+            keep |= p.grouped[int64_t(g) * p.T + p.col[task.x + k]] == 0;
+          p.fflag[p.toff[e] + i] = keep;
         }
       }
     }
     __syncthreads();
+  }
+  if (PASS != kPassEmit) {
+    if (my_nsel) atomicAdd(&s_nsel[oct], my_nsel);
+    if (my_bad) atomicOr(&s_bad, 1u << oct);
+    if (my_pdiff) atomicOr(&s_pdiff, 1u << (oct >> 1));
+    __syncthreads();
+    auto uniform = [&](int o) {
+      return octet_rows(o) > 0 && s_nsel[o] > 0 && !((s_bad >> o) & 1u);
+    };
+    auto paired = [&](int i) {
+      return uniform(2 * i) && uniform(2 * i + 1) && !((s_pdiff >> i) & 1u);
+    };
+    if (PASS == kPassCount && valid)
+      p.grouped[int64_t(g) * p.T + t] = uniform(r >> 3) ? 1 : 0;
+    const int o = r >> 3;
+    if ((r & 7) == 0 && uniform(o) && !((o & 1) && paired(o >> 1))) {
+      const bool hasB = !(o & 1) && paired(o >> 1);
+      const int cost = s_nsel[o] * (hasB ? 2 : 1);
+      unsigned long long* cnt = reinterpret_cast<unsigned long long*>(hdr + kHdrCost);
+      if (PASS == kPassCount) {
+        atomicAdd(cnt + cost, 1ull);
+      } else {
+        int64_t pos = 0;  // items of higher cost come first
+        for (int c = cost + 1; c <= kMaxItemCost; ++c) pos += hdr[kHdrCost + c];
+        pos += int64_t(atomicAdd(
+            reinterpret_cast<unsigned long long*>(hdr + kHdrCostFill) + cost, 1ull));
+        int32_t* it = p.items + pos * kItemWords;
+        *reinterpret_cast<int4*>(it) =
+            make_int4(int32_t(t), hasB ? int32_t(t + 8) : -1,
+                      octet_rows(o) | (hasB ? octet_rows(o + 1) : 0) << 4 | g << 8 |
+                          s_nsel[o] << 12,
+                      d);
+        // this query's visible blocks (distinct after the dedupe), ascending
+        int nb = 0;
+#pragma unroll
+        for (int i = 0; i < kTopK; ++i) {
+          if (sl[i] < 0 || sl[i] > qb) continue;
+          int rank = 0;
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) rank += (sl[j] >= 0 && sl[j] < sl[i]);
+          it[4 + rank] = sl[i];
+          ++nb;
+        }
+        for (int k = nb; k < kTopK; ++k) it[4 + k] = -1;
+      }
+    }
+    if (PASS == kPassScatter && blockIdx.x == 0 && threadIdx.x == 0) {
+      int64_t tot = 0;
+      for (int c = 1; c <= kMaxItemCost; ++c) tot += hdr[kHdrCost + c];
+      hdr[kHdrItems] = tot;
+    }
   }
   if (PASS == kPassScatter) {
     if (pairs) atomicAdd(&s_pairs, (unsigned long long)pairs);
@@ -318,6 +408,14 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_down(const int32_t* in, i
   }
 }
 
+// The forward's pooled task list: tasks with fflag set, in task order.
+__global__ void __launch_bounds__(256) k_ftask_scatter(msa_plan p) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (plan_failed(p.header) || i >= p.header[kHdrTasks]) return;
+  if (p.fflag[i])
+    reinterpret_cast<int4*>(p.ftasks)[p.fpos[i]] = reinterpret_cast<const int4*>(p.tasks)[i];
+}
+
 cudaError_t scan(const int32_t* in, int32_t* out, const int64_t* n_ptr, int64_t cap,
                  int32_t* tmp, int64_t* total, cudaStream_t s) {
   const unsigned grid = unsigned((cap + kScanTile - 1) / kScanTile);
@@ -351,6 +449,12 @@ cudaError_t launch_plan(const msa_plan& p, cudaStream_t s) {
   launch_begin("plan_emit", s);
   k_plan_blocks<kPassEmit><<<grid, 128, 0, s>>>(p);
   launch_end("plan_emit", s);
+  e = scan(p.fflag, p.fpos, p.header + kHdrTasks, p.task_cap, p.scan_tmp,
+           p.header + kHdrFTasks, s);
+  if (e != cudaSuccess) return e;
+  launch_begin("plan_ftasks", s);
+  k_ftask_scatter<<<unsigned((p.task_cap + 255) / 256), 256, 0, s>>>(p);
+  launch_end("plan_ftasks", s);
   return cudaGetLastError();
 }
 

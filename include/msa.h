@@ -146,6 +146,15 @@ typedef struct msa_plan {
   int32_t* tasks;     /* device: [task_cap][4] task records                 */
   int32_t* scan_tmp;  /* device: scan scratch                               */
   int64_t scan_tmp_len;
+  /* The forward's octet groups: aligned runs of 8 tokens (document positions
+   * 8k .. 8k+7) whose tokens all see the same selected blocks; their tiles
+   * are accumulated block after block in one place, without the pool. */
+  int64_t item_cap;   /* bound on octet-group items                        */
+  uint8_t* grouped;   /* device: [4][T] 1 = the token's octet is grouped    */
+  int32_t* items;     /* device: [item_cap][20] group items (msa_plan_export_groups) */
+  int32_t* fflag;     /* device: [task_cap] task has an ungrouped query      */
+  int32_t* fpos;      /* device: [task_cap] exclusive prefix of fflag        */
+  int32_t* ftasks;    /* device: [task_cap][4] the forward's pooled tasks    */
 } msa_plan;
 
 /* Bytes of plan workspace needed for T tokens in num_docs documents.
@@ -228,7 +237,8 @@ msa_status msa_read_status(const msa_plan* plan, msa_stream_t stream);
 
 /* Plan counts after synchronising the stream: counts[0] = key blocks NB,
  * [1] = CSR entries, [2] = tasks, [3] = attended (query, head, key) triples,
- * [4] = count entries.  Host array of 5 int64. */
+ * [4] = count entries, [5] = octet-group items, [6] = tasks of the forward's
+ * pooled list.  Host array of 7 int64. */
 msa_status msa_plan_counts(const msa_plan* plan, msa_stream_t stream, int64_t* counts);
 
 /*
@@ -242,6 +252,24 @@ msa_status msa_plan_counts(const msa_plan* plan, msa_stream_t stream, int64_t* c
  */
 msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* col,
                            int64_t col_capacity, int32_t* tasks, int64_t task_capacity);
+
+/*
+ * Copy the forward's octet-group tables to host memory after synchronising
+ * the stream (for the plan tests).  Each destination may be NULL to skip it.
+ *   grouped uint8 [4][T]: 1 where the token's octet is grouped
+ *   items   int32 [n_items][20]: first token of octet A, of octet B (-1 if
+ *           none), queries of A | of B << 4 | index head << 8 | blocks << 12,
+ *           document index, then the blocks ascending (-1 padded); items are
+ *           ordered by decreasing work (blocks x octets)
+ *   ftasks  int32 [n_ftasks][4]: the task records (as in msa_plan_export) of
+ *           the tasks with at least one ungrouped query, in task order
+ * Capacities are element counts of the first dimension (T for grouped, which
+ * must be >= T); too small -> MSA_ERR_INVALID_ARG.
+ */
+msa_status msa_plan_export_groups(const msa_plan* plan, msa_stream_t stream, uint8_t* grouped,
+                                  int64_t grouped_capacity, int32_t* items,
+                                  int64_t item_capacity, int32_t* ftasks,
+                                  int64_t ftask_capacity);
 
 /*
  * Compaction of padded packed rows into the compact THD layout, and back

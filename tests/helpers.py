@@ -67,3 +67,19 @@ def canonical_oracle_plan(pl):
     tasks = sorted(((int(b), tuple(int(x) for x in col[first:first + n]))
                     for b, first, n in pl["tasks"]), key=lambda x: (x[0], x[1][0]))
     return buckets, tasks
+
+
+def canonical_items(items, blocks_at):
+    """Octet-group items -> sorted [(g, tokA, tokB, nqA, nqB, nsel, blocks...)].
+    GPU rows: tokA, tokB, nqA | nqB << 4 | g << 8 | nsel << 12, doc, blocks
+    (blocks_at=4); oracle rows: tokA, tokB, nqA, nqB, g, nsel, blocks (6)."""
+    out = []
+    for r in items:
+        r = [int(x) for x in r]
+        if blocks_at == 4:
+            z = r[2]
+            key = (z >> 8 & 3, r[0], r[1], z & 0xF, z >> 4 & 0xF, z >> 12 & 0x1F)
+        else:
+            key = (r[4], r[0], r[1], r[2], r[3], r[5])
+        out.append(key + tuple(r[blocks_at:blocks_at + 16]))
+    return sorted(out)

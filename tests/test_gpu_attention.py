@@ -128,6 +128,25 @@ def test_fp16_dq_pool_overflow_is_reported():
     assert api.msa_read_status(plan) == 0
 
 
+@pytest.mark.parametrize("name", ["multidoc-ragged", "cfg1-dense-causal"])
+def test_large_v_values(name):
+    # V of KV head 2 scaled by 2^20 (exact in bf16): above the fp16 range of
+    # the P.V products, so the forward scales that head's fp16 copy of V and
+    # multiplies O back.  O of heads 32-47 scales by 2^20 exactly; LSE does
+    # not change.  Covers the pooled tasks (random selections) and the
+    # grouped octets (the dense causal case).
+    w, O, L, *_ = oracle_results(name)
+    v = w.v.clone()
+    v[:, 2, :] = (v[:, 2, :].float() * 2.0 ** 20).to(torch.bfloat16)
+    plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=16)
+    o, lse = api.msa_forward(plan, w.q.to(DEV), w.k.to(DEV), v.to(DEV), w.scale)
+    assert api.msa_read_status(plan) == 0
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    o[:, 32:48] /= 2.0 ** 20
+    check_o(o, O)
+    check_lse(lse, L)
+
+
 def test_rows_without_keys_are_zero():
     w, O, L, dQ, *_ = oracle_results("edge")
     o, lse, dq, _, _ = run_gpu(w)

@@ -1,14 +1,16 @@
 """GPU plan builder vs the oracle's canonical k2q CSR and task table: bit-exact
 after canonical ordering, on all five workload structures and irregular
 selections (duplicates, -1 slots, future blocks, one-token documents, partial
-last blocks), for several super-block lengths; plus device-side validation."""
+last blocks), for several super-block lengths; the forward's octet groups
+(grouped flags bit-exact, items and the pooled task list after canonical
+ordering, items in non-increasing cost); plus device-side validation."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from block_sparse_gqa_msa_gb300 import api, inputs
-from tests.helpers import canonical_gpu_plan, canonical_oracle_plan
+from tests.helpers import canonical_gpu_plan, canonical_items, canonical_oracle_plan
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +55,23 @@ def _check(lens, q2k, Z):
     assert (cover == 1).all()
     n = oracle.pair_count(q2k, offs, T)
     assert counts["pairs"] == n
+    # the forward's octet groups
+    grouped, items, ftasks = api.msa_plan_export_groups(plan)
+    og = oracle.groups(q2k, offs, T)
+    assert np.array_equal(grouped, og["grouped"])
+    assert counts["items"] == len(og["items"])
+    assert canonical_items(items, 4) == canonical_items(og["items"], 6)
+    cost = (items[:, 2] >> 12 & 0x1F) * np.where(items[:, 1] >= 0, 2, 1)
+    assert (np.diff(cost) <= 0).all()
+    oft = oracle.forward_tasks(pl, og["grouped"])
+    assert counts["ftasks"] == len(oft)
+    _, gft = canonical_gpu_plan(col, ftasks, offs, pl["NB"])
+    _, oft_c = canonical_oracle_plan(dict(pl, tasks=oft))
+    assert gft == oft_c
+    # the pooled list keeps the task order
+    keep = [i for i, (first, _, z, _) in enumerate(tasks)
+            if not grouped[(z >> 12) & 3, col[first:first + ((z >> 8) & 0xF)]].all()]
+    assert np.array_equal(ftasks, tasks[keep])
 
 
 @pytest.mark.parametrize("name", list(STRUCTURES))
