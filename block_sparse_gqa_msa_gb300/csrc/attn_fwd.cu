@@ -27,8 +27,9 @@
 //
 // Kernels, in launch order:
 //   fwd_kmax      per (index head, key block): max key norm, max |v|
-//   fwd_rows      per ungrouped (token, index head): row shifts M, zero the pool
+//   fwd_v16       V as fp16 for the P.V products
 //   fwd_group     grouped octets: block walk with O in tensor memory
+//   fwd_rows      per ungrouped (token, index head): row shifts M, zero the pool
 //   fwd_main      the pooled task loop (TMA + tcgen05 + TMEM)
 //   fwd_finalize  pooled rows: O = pool / sum -> bf16, LSE; flags underflow
 //   fwd_fallback  exact recomputation of the flagged rows (usually none)
@@ -1407,11 +1408,6 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   k_fwd_v16<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(
       p, static_cast<const __nv_bfloat16*>(v), vmax, v16, vscale);
   launch_end("fwd_v16", s);
-  const int64_t warps = p.T * kKVHeads;
-  launch_begin("fwd_rows", s);
-  k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
-  launch_end("fwd_rows", s);
 
   static bool attr_set = false;
   if (!attr_set) {
@@ -1424,9 +1420,17 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   FwdParams prm{p,    M2,   kmax, vmax, pool, lsum, list, static_cast<__nv_bfloat16*>(o),
                 lse,  vscale, c2};
   const unsigned grid = unsigned(device_sm_count());
+  // The group kernel needs neither the row shifts nor the pool: it runs
+  // first, on the K / V / Q lines the earlier kernels left in L2.
   launch_begin("fwd_group", s);
   k_fwd_group<<<grid, kGrpThreads, kGrpSmem, s>>>(prm, mQ, mK, mV);
   launch_end("fwd_group", s);
+  const int64_t warps = p.T * kKVHeads;
+  launch_begin("fwd_rows", s);
+  k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
+      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
+  launch_end("fwd_rows", s);
+
   launch_begin("fwd_main", s);
   k_fwd_main<<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
   launch_end("fwd_main", s);
