@@ -36,7 +36,22 @@ def _stale(out: str, deps: list[str]) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+    """The product library, libmsa.so."""
+    return _build(BUILD, LIB, [], force, verbose)
+
+
+def build_starve(force: bool = False, verbose: bool = False) -> str:
+    """A TEST-ONLY variant of the library, never used by the product: bounded
+    pipeline waits give up after 2 ms instead of 1 s, and msa_test_starve(k)
+    makes CTA 0 of one kernel leave out its first Q tile, so that the tests
+    can drive the timeout path.  Built into _build/starve/."""
+    d = os.path.join(BUILD, "starve")
+    return _build(d, os.path.join(d, "libmsa_starve.so"),
+                  ["-DMSA_TEST_STARVE", "-DMSA_WAIT_TIMEOUT_NS=2000000ull"], force, verbose)
+
+
+def _build(out_dir: str, lib: str, defines: list[str], force: bool, verbose: bool) -> str:
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
@@ -44,10 +59,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers, __file__]):
-            jobs.append([nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj])
+            jobs.append([nvcc, *ARCH, *NVCC_FLAGS, *defines, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,10 +73,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-lcudart_static", "-ldl", "-lrt",
+    if force or jobs or _stale(lib, objs):
+        run([nvcc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart_static", "-ldl", "-lrt",
              "-lpthread"])
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -37,6 +37,17 @@
 #include <type_traits>
 
 namespace msa {
+
+#ifdef MSA_TEST_STARVE
+// Test-only build: when set (3), CTA 0 of bwd_main leaves out its first
+// Q / dO tiles, so that a bounded wait runs out and the call reports
+// MSA_ERR_TIMEOUT.  Set by msa_test_starve.
+__device__ int g_starve_bwd;
+cudaError_t test_set_starve_bwd(int which) {
+  return cudaMemcpyToSymbol(g_starve_bwd, &which, sizeof which);
+}
+#endif
+
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -443,6 +454,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (it >= 2 &&
             !mbar_wait(smem_u32(&bars.qdo_empty[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
           break;
+#ifdef MSA_TEST_STARVE
+        if (!(g_starve_bwd == 3 && blockIdx.x == 0 && it == 0)) {
+#endif
         const uint32_t b = smem_u32(&bars.qdo_full[st]);
         mbar_arrive_expect_tx(b, 2 * kTileBytes);
         const uint32_t dq = sbase + kSmQ + st * kTileBytes, dd = sbase + kSmDO + st * kTileBytes;
@@ -454,6 +468,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_2d(dd + qi * 2048, &mapDO, b, 0, y);
           tma_load_2d(dd + 16384 + qi * 2048, &mapDO, b, 64, y);
         }
+#ifdef MSA_TEST_STARVE
+        }
+#endif
         rec = rec1;
         rec1 = rec2;
 #pragma unroll

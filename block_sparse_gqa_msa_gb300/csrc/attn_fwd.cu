@@ -37,6 +37,17 @@
 #include "sm100.cuh"
 
 namespace msa {
+
+#ifdef MSA_TEST_STARVE
+// Test-only build: the kernel whose CTA 0 leaves out its first Q tile (1:
+// fwd_group, 2: fwd_main, 0: none), so that a bounded wait runs out and the
+// call reports MSA_ERR_TIMEOUT.  Set by msa_test_starve.
+__device__ int g_starve_fwd;
+cudaError_t test_set_starve_fwd(int which) {
+  return cudaMemcpyToSymbol(g_starve_fwd, &which, sizeof which);
+}
+#endif
+
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -619,9 +630,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             !mbar_wait(smem_u32(&bars.q_empty[st]), uint32_t(((it >> 1) - 1) & 1), abort_flag))
           break;
 #ifdef MSA_TEST_STARVE
-        // test-only build: CTA 0 never loads its first Q tile, so the MMA
-        // issuer's bounded wait for it runs out
-        if (!(blockIdx.x == 0 && it == 0))
+        if (!(g_starve_fwd == 2 && blockIdx.x == 0 && it == 0))
 #endif
         {
           const uint32_t b = smem_u32(&bars.q_full[st]);
@@ -1083,9 +1092,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             !mbar_wait(smem_u32(&bars.q_empty[buf]), uint32_t((qu[buf] - 1) & 1), abort_flag))
           return false;
 #ifdef MSA_TEST_STARVE
-        // test-only build: CTA 0 never loads its first Q tile, so the waits
-        // for it run out
-        if (blockIdx.x == 0 && buf == 0 && qu[0] == 0) {
+        if (g_starve_fwd == 1 && blockIdx.x == 0 && buf == 0 && qu[0] == 0) {
           ++qu[buf];
           return true;
         }

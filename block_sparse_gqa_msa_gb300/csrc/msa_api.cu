@@ -182,6 +182,22 @@ CUresult make_map_pool32(CUtensorMap* m, const void* base, int64_t rows) {
 
 using namespace msa;
 
+#ifdef MSA_TEST_STARVE
+namespace msa {
+cudaError_t test_set_starve_fwd(int which);  // attn_fwd.cu
+cudaError_t test_set_starve_bwd(int which);  // attn_bwd.cu
+}  // namespace msa
+// Test-only build: make CTA 0 of one kernel (1: fwd_group, 2: fwd_main,
+// 3: bwd_main, 0: none) leave out its first Q tile, so that a bounded
+// pipeline wait runs out and the call reports MSA_ERR_TIMEOUT.
+extern "C" msa_status msa_test_starve(int32_t which) {
+  if (which < 0 || which > 3) return MSA_ERR_INVALID_ARG;
+  if (test_set_starve_fwd(which) != cudaSuccess || test_set_starve_bwd(which) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+#endif
+
 // ------------------------------------------------------------ C ABI
 extern "C" {
 

@@ -16,7 +16,11 @@
 namespace msa {
 
 // One second of global time: a healthy pipeline stage never waits that long.
-constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+// (A test-only build shortens it with -DMSA_WAIT_TIMEOUT_NS=...)
+#ifndef MSA_WAIT_TIMEOUT_NS
+#define MSA_WAIT_TIMEOUT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitTimeoutNs = MSA_WAIT_TIMEOUT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
