@@ -122,6 +122,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+// The library runs on sm_100 / sm_103 class devices only (also used by
+// plan_static.cu).
 msa_status check_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
@@ -130,9 +136,6 @@ msa_status check_device() {
     return MSA_ERR_CUDA;
   return major == 10 ? MSA_OK : MSA_ERR_UNSUPPORTED;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-}  // namespace
 
 // [rows, 128] bf16 rows (Q or dO viewed as [T*64, 128]); box = 16 rows x 64
 // columns, 128-byte swizzle: one box is the 16 heads of one index head of

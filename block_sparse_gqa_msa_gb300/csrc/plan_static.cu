@@ -5,39 +5,20 @@
 // framework hook that receives only the input buffers).
 //
 // The scratch is one file-scope __device__ array of kStaticPlanBytes; every
-// GPU that loads the library holds it until the process exits.  Its address
-// is looked up once per device with cudaGetSymbolAddress (host code may not
-// use the array's name as a device pointer).
-#include <map>
-#include <mutex>
-
+// GPU that loads the library holds it until the process exits.  Host code
+// may not use the array's name as a device pointer: its address on the
+// current device is looked up with cudaGetSymbolAddress on every call (cheap
+// after the first), so a device reset followed by another call still finds
+// the live address.
 #include "common.cuh"
 
 namespace msa {
+msa_status check_device();  // msa_api.cu
+
 namespace {
 
 constexpr size_t kStaticPlanBytes = size_t(16) << 20;  // 16 MiB
 __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
-
-std::mutex g_static_mu;
-std::map<int, void*> g_static_addr;  // device ordinal -> device address of g_static_plan
-
-// Device address of the scratch array on the current device (looked up on
-// the first call per device).  Returns nullptr if the lookup fails.
-void* static_plan_scratch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  std::lock_guard<std::mutex> g(g_static_mu);
-  auto it = g_static_addr.find(dev);
-  if (it != g_static_addr.end()) return it->second;
-  void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_static_plan) != cudaSuccess || ptr == nullptr) {
-    cudaGetLastError();  // clear the error so later runtime calls do not report it
-    return nullptr;
-  }
-  g_static_addr[dev] = ptr;
-  return ptr;
-}
 
 }  // namespace
 }  // namespace msa
@@ -49,8 +30,11 @@ extern "C" msa_status msa_build_plan_static(const int32_t* q2k, const int32_t* d
   if (!q2k || !doc_offsets || !out) return MSA_ERR_INVALID_ARG;
   if (T < 1 || T > msa::kMaxTokens || num_docs < 1 || num_docs > T) return MSA_ERR_INVALID_ARG;
   if (msa::plan_layout(T, num_docs).total > msa::kStaticPlanBytes) return MSA_ERR_WORKSPACE;
-  void* scratch = msa::static_plan_scratch();
-  if (!scratch) return MSA_ERR_CUDA;
+  const msa_status dev = msa::check_device();
+  if (dev != MSA_OK) return dev;
+  void* scratch = nullptr;
+  if (cudaGetSymbolAddress(&scratch, msa::g_static_plan) != cudaSuccess || !scratch)
+    return MSA_ERR_CUDA;
   return msa_build_plan(q2k, doc_offsets, T, num_docs, opts, scratch, msa::kStaticPlanBytes,
                         stream, out);
 }

@@ -183,12 +183,14 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
  * memory manager that forbids allocation at that point, a hook that is handed
  * only the input buffers).  The pages have no counterpart of this call.
  *   - The tables live in one static 16 MiB device array that every GPU which
- *     loads the library keeps until the process exits; T and num_docs whose
- *     msa_plan_workspace_bytes exceeds 16 MiB are rejected with
- *     MSA_ERR_WORKSPACE (roughly T <= 16384 tokens; the exact bound depends on
- *     the number of documents).
- *   - The first call on a device looks the array up (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *     loads the library keeps until the process exits.  A problem is
+ *     accepted while msa_plan_workspace_bytes(T, num_docs) <= 16 MiB (about
+ *     T <= 21600 tokens, a little more or less with the number of
+ *     documents); larger ones are rejected with MSA_ERR_WORKSPACE after the
+ *     argument checks and before any CUDA call.
+ *   - Each call looks the array's device address up on the current device
+ *     (cudaGetSymbolAddress); the first call on a device initialises the
+ *     library's module there, so make it before any stream capture.
  *   - Every call reuses the same array: the returned plan is valid until the
  *     next msa_build_plan_static call on that device, and calls (or uses of
  *     the plan) that overlap on the GPU race.  Nothing else is allocated.

@@ -165,3 +165,33 @@ def test_struct_layouts_match_header():
     assert {k: got[("enum", "MSA_DQ_ACCUM_" + k.upper())] for k in api.DQ_ACCUM} == api.DQ_ACCUM
     assert {k: got[("enum", "MSA_O_ACCUM_" + k.upper())] for k in api.O_ACCUM} == api.O_ACCUM
 
+
+
+def _static_limit(lib, D):
+    """Largest T whose plan workspace fits the static plan array (16 MiB)."""
+    def ws(T):
+        n = ctypes.c_size_t(0)
+        assert lib.msa_plan_workspace_bytes(T, D, ctypes.byref(n)) == 0
+        return n.value
+    lo, hi = D, 1 << 20
+    while lo < hi:
+        m = (lo + hi + 1) // 2
+        if ws(m) <= 16 << 20:
+            lo = m
+        else:
+            hi = m - 1
+    return lo
+
+
+def test_build_plan_static_host_checks(lib):
+    st = api.MsaPlanStruct()
+    g = ctypes.c_void_p(0x10000)
+    assert lib.msa_build_plan_static(None, g, 1000, 2, None, None, ctypes.byref(st)) == 1
+    assert lib.msa_build_plan_static(g, g, 1000, 2, None, None, None) == 1
+    assert lib.msa_build_plan_static(g, g, 0, 1, None, None, ctypes.byref(st)) == 1
+    assert lib.msa_build_plan_static(g, g, 10, 11, None, None, ctypes.byref(st)) == 1
+    for D in (1, 7, 64):
+        t_max = _static_limit(lib, D)
+        assert 20000 < t_max < 23000
+        # one token more no longer fits: rejected before any CUDA call
+        assert lib.msa_build_plan_static(g, g, t_max + 1, D, None, None, ctypes.byref(st)) == 4
