@@ -308,6 +308,57 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- streaming kernels
+def streaming_bytes(T: int, n_ungrouped: int, dq_esz: int = 2) -> dict:
+    """Algorithmic bytes per launch of the HBM-bound kernels: what each must
+    read and write by its definition (n_ungrouped: (token, index head) pairs
+    whose octet is not grouped; dq_esz: bytes per dQ pool element)."""
+    kv = T * 4 * 128 * 2  # one of K, V as bf16
+    rows_q = T * 64 * 128 * 2  # one of Q, O, dO as bf16
+    return {
+        "fwd_kmax": 2 * kv,                                  # K, V read
+        "fwd_v16": 2 * kv,                                   # V read, fp16 V written
+        "fwd_rows": n_ungrouped * (4096 + 64 + 128 + 8192),  # Q, q2k read; shifts, sums, pool zeroed
+        "fwd_finalize": n_ungrouped * (8192 + 128 + 4096 + 64),  # pool, shifts, sums read; O, LSE
+        "bwd_delta": 2 * rows_q + T * 64 * 4 + T * 64 * 128 * dq_esz + 2 * T * 512 * 4,
+        "bwd_finalize": T * 64 * 128 * dq_esz + 2 * T * 512 * 4 + rows_q + 2 * kv,
+    }
+
+
+def measure_workload(api, dev, n: int, steps: int = 5) -> dict:
+    """plan + forward + backward of workload n with inputs resident and L2
+    flushed before each timed step: TFLOP/s of the method's FLOPs."""
+    w = inputs.config(n)
+    q, k, v, do = (x.to(dev) for x in (w.q, w.k, w.v, w.do))
+    q2k, offs = w.q2k.to(dev), w.doc_offsets.to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        p = api.msa_build_plan(q2k, offs)
+        o, lse = api.msa_forward(p, q, k, v, w.scale)
+        api.msa_backward(p, q, k, v, o, lse, do, w.scale)
+        return p
+
+    for _ in range(3):
+        p = step()
+    torch.cuda.synchronize()
+    pairs = api.msa_plan_counts(p)["pairs"]
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    m = statistics.mean(ms)
+    flop = pairs * (FWD_FLOP_PER_PAIR + BWD_FLOP_PER_PAIR)
+    return {"workload": w.name, "T": w.T, "ms_per_step": m, "TFLOP_s": flop / (m * 1e-3) / 1e12,
+            "steps": steps}
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world):
     from block_sparse_gqa_msa_gb300 import api
@@ -466,6 +517,25 @@ def run_gpu(args, rank, world):
     traffic = recorded_traffic(dom, w.name)
 
     adjacent = measure_packing(dev, peaks) if not args.no_adjacent else None
+    if adjacent is not None and WORKLOAD != 2:
+        # the pages' own operator benchmark setting: one document of 16k tokens
+        adjacent["single_doc_16k"] = measure_workload(api, dev, 2)
+        adjacent["single_doc_16k"]["pct_of_peak"] = (
+            100.0 * adjacent["single_doc_16k"]["TFLOP_s"] / float(peaks["bf16_tflops"]))
+    # HBM-bound kernels: algorithmic bytes per launch against the copy bandwidth
+    grouped, _, _ = api.msa_plan_export_groups(plan)
+    sbytes = streaming_bytes(T, int((grouped == 0).sum()))
+    streaming = {}
+    for name, nbytes in sbytes.items():
+        if name in kern:
+            ms_l = kern[name]["ms_per_step"] * args.steps / kern[name]["launches"]
+            gbs = nbytes / (ms_l * 1e-3) / 1e9
+            streaming[name] = {"bytes": nbytes, "ms": round(ms_l, 4), "GB_s": round(gbs, 1),
+                               "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 3)}
+    # the main kernels' times in clock cycles (box-to-box comparisons at equal work)
+    mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    mcycles = {n_: round(kern[n_]["ms_per_step"] * args.steps / kern[n_]["launches"] * mhz / 1e3, 3)
+               for n_ in ("fwd_group", "fwd_main", "bwd_main") if n_ in kern}
     cpu = cpu_sample(w, budget_s=20.0) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -482,6 +552,8 @@ def run_gpu(args, rank, world):
         "ms": {"plan": statistics.mean(plan_ms), "fwd": statistics.mean(fwd_ms),
                "bwd": statistics.mean(bwd_ms)},
         "kernels_ms_per_step": {k_: round(v_["ms_per_step"], 4) for k_, v_ in kern.items()},
+        "kernels_mcycles_per_launch": mcycles,
+        "streaming": streaming,
         "clocks": clk,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
