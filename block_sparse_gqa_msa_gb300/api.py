@@ -40,7 +40,8 @@ class MSAError(RuntimeError):
 class MsaPlanStruct(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int64), ("num_docs", ctypes.c_int32), ("super_block", ctypes.c_int32),
-        ("dq_accum", ctypes.c_int32), ("o_accum", ctypes.c_int32), ("nb_cap", ctypes.c_int64), ("tri_cap", ctypes.c_int64), ("nnz_cap", ctypes.c_int64),
+        ("dq_accum", ctypes.c_int32), ("o_accum", ctypes.c_int32),
+        ("dense_blocks", ctypes.c_int32), ("nb_cap", ctypes.c_int64), ("tri_cap", ctypes.c_int64), ("nnz_cap", ctypes.c_int64),
         ("task_cap", ctypes.c_int64),
         ("q2k", ctypes.c_void_p), ("doc_offsets", ctypes.c_void_p), ("header", ctypes.c_void_p),
         ("doc_info", ctypes.c_void_p), ("doc_tri", ctypes.c_void_p), ("cnt", ctypes.c_void_p),
@@ -54,7 +55,8 @@ class MsaPlanStruct(ctypes.Structure):
 
 class MsaPlanOptions(ctypes.Structure):
     _fields_ = [("super_block", ctypes.c_int32), ("dq_accum", ctypes.c_int32),
-                ("o_accum", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("o_accum", ctypes.c_int32), ("dense_blocks", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
 
 
 DQ_ACCUM = {"f16": 0, "bf16": 1, "f32": 2}
@@ -171,11 +173,13 @@ def plan_workspace_bytes(T: int, num_docs: int) -> int:
 
 def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 64,
                    workspace: torch.Tensor | None = None, stream=None,
-                   dq_accum: str = "f16", o_accum: str = "f32") -> Plan:
+                   dq_accum: str = "f16", o_accum: str = "f32", dense_blocks: int = 0) -> Plan:
     """Device-side plan from q2k int32 [4,T,16] and doc_offsets int32 [D+1].
     dq_accum: precision of the backward's dQ pool ("f16", "bf16" or "f32");
     o_accum: precision of the forward's O pool (only "f32" is accepted; the
-    library rejects "bf16", whose O error exceeds the forward's bar)."""
+    library rejects "bf16", whose O error exceeds the forward's bar);
+    dense_blocks: bound on the query block (b + 1 <= dense_blocks) of the
+    forward's dense octets (0: the default, 28; -1: none)."""
     if q2k.dim() != 3:
         raise ValueError("q2k must be [4, T, 16]")
     T = int(q2k.shape[1])
@@ -186,7 +190,7 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q2k.device)
     opts = MsaPlanOptions(super_block=super_block, dq_accum=DQ_ACCUM[dq_accum],
-                          o_accum=O_ACCUM[o_accum])
+                          o_accum=O_ACCUM[o_accum], dense_blocks=dense_blocks)
     st = MsaPlanStruct()
     _check(lib().msa_build_plan(_ptr(q2k), _ptr(doc_offsets), T, D, ctypes.byref(opts),
                                 _ptr(workspace), workspace.numel(), _stream(stream),
@@ -195,7 +199,8 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
 
 
 def msa_build_plan_static(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: int = 64,
-                          stream=None, dq_accum: str = "f16", o_accum: str = "f32") -> Plan:
+                          stream=None, dq_accum: str = "f16", o_accum: str = "f32",
+                          dense_blocks: int = 0) -> Plan:
     """Like msa_build_plan, but the plan tables live in the library's own
     static device array, so nothing is allocated.  For callers that cannot
     allocate device memory; the plan is valid until the next call."""
@@ -206,7 +211,7 @@ def msa_build_plan_static(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_bl
     _need(q2k, "q2k", torch.int32, (NUM_KV_HEADS, T, TOPK))
     _need(doc_offsets, "doc_offsets", torch.int32, (D + 1,))
     opts = MsaPlanOptions(super_block=super_block, dq_accum=DQ_ACCUM[dq_accum],
-                          o_accum=O_ACCUM[o_accum])
+                          o_accum=O_ACCUM[o_accum], dense_blocks=dense_blocks)
     st = MsaPlanStruct()
     _check(lib().msa_build_plan_static(_ptr(q2k), _ptr(doc_offsets), T, D, ctypes.byref(opts),
                                        _stream(stream), ctypes.byref(st)), "msa_build_plan_static")

@@ -89,11 +89,22 @@ __device__ __forceinline__ int doc_of_token(const int32_t* offs, int D, int64_t 
 }
 
 // ------------------------------------------------------------ fwd_kmax
-// kmax[g * nb_cap + b] = max over the keys j of global block b of |K[j,g]|.
-__global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat16* K,
-                                                  const __nv_bfloat16* V, float* kmax,
-                                                  float* vmax, int32_t* list) {
-  __shared__ float red[4][4], redv[4][4];
+// One CTA per global key block b (its 128 keys x 4 KV heads are 128 KB of K
+// and of V, contiguous):
+//   kmax[g * nb_cap + b] = max over the block's keys j of |K[j,g]|,
+//   vmax[g * nb_cap + b] = max over them of |V[j,g,d]|,
+// and V[j,g] converted to fp16 into the forward's copy, unscaled (fwd_v16
+// rescales the copy in the rare case that some |v| exceeds 2^15).  Sixteen
+// lanes read one 256-byte (key, head) row, so every warp access is 512
+// contiguous bytes; a thread's rows all belong to one head.
+constexpr int kKmaxThreads = 512;
+__global__ void __launch_bounds__(kKmaxThreads) k_fwd_kmax(msa_plan p, const __nv_bfloat16* K,
+                                                           const __nv_bfloat16* V, float* kmax,
+                                                           float* vmax, int32_t* list,
+                                                           uint4* v16) {
+  constexpr int kRowsPerPass = kKmaxThreads / 16;              // 32 rows per pass
+  constexpr int kPasses = kBlock * kKVHeads / kRowsPerPass;    // 16 passes
+  __shared__ float hk[kRowsPerPass], hv[kRowsPerPass];
   if (blockIdx.x == 0 && threadIdx.x == 0) list[0] = 0;  // fallback row count
   const int64_t NB = p.header[kHdrNB];
   const int64_t gb = blockIdx.x;
@@ -106,63 +117,69 @@ __global__ void __launch_bounds__(128) k_fwd_kmax(msa_plan p, const __nv_bfloat1
   }
   const DocInfo di = info[lo];
   const int64_t kb = (gb - di.blk_base) * kBlock;
-  const int r = threadIdx.x;
-  float nrm[4] = {0.f, 0.f, 0.f, 0.f}, vm[4] = {0.f, 0.f, 0.f, 0.f};
-  if (kb + r < di.len) {
-    const int64_t j = di.start + kb + r;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const uint4* src = reinterpret_cast<const uint4*>(K + (j * kKVHeads + g) * kHeadDim);
-      const uint4* vsrc = reinterpret_cast<const uint4*>(V + (j * kKVHeads + g) * kHeadDim);
-      float s = 0.f, m = 0.f;
+  const int nkeys = int(di.len - kb < kBlock ? di.len - kb : kBlock);
+  const int c = threadIdx.x & 15;        // 16-byte chunk of the row
+  const int r0 = threadIdx.x >> 4;       // row slot: rows r0 + 32 pass, all of head r0 % 4
+  const int64_t base = (di.start + kb) * kKVHeads * (kHeadDim / 8);  // block's first chunk
+  const uint4* ksrc = reinterpret_cast<const uint4*>(K) + base;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(V) + base;
+  uint4* vdst = v16 + base;
+  float nrm = 0.f, vm = 0.f;
 #pragma unroll 4
-      for (int c = 0; c < 16; ++c) {
-        const uint4 x = src[c];
-        const uint4 y = vsrc[c];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        const uint32_t u[4] = {y.x, y.y, y.z, y.w};
+  for (int ps = 0; ps < kPasses; ++ps) {
+    const int row = ps * kRowsPerPass + r0;   // key row / 4, head row % 4
+    const bool ok = (row >> 2) < nkeys;
+    const int64_t i = int64_t(row) * 16 + c;
+    const uint4 x = ok ? ksrc[i] : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 y = ok ? vsrc[i] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    const uint32_t u[4] = {y.x, y.y, y.z, y.w};
+    float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
-          s = fmaf(a, a, s);
-          s = fmaf(b, b, s);
-          m = fmaxf(m, fmaxf(fabsf(bf16_lo(u[e])), fabsf(bf16_hi(u[e]))));
-        }
-      }
-      nrm[g] = sqrtf(s);
-      vm[g] = m;
+    for (int e = 0; e < 4; ++e) {
+      const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+      ss = fmaf(a, a, fmaf(b, b, ss));
+      vm = fmaxf(vm, fmaxf(fabsf(bf16_lo(u[e])), fabsf(bf16_hi(u[e]))));
     }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    nrm = fmaxf(nrm, sqrtf(ss));
+    if (ok)
+      vdst[i] = make_uint4(pack_f16x2(bf16_lo(u[0]), bf16_hi(u[0])),
+                           pack_f16x2(bf16_lo(u[1]), bf16_hi(u[1])),
+                           pack_f16x2(bf16_lo(u[2]), bf16_hi(u[2])),
+                           pack_f16x2(bf16_lo(u[3]), bf16_hi(u[3])));
   }
+  // per row slot r0 (head r0 % 4): the max over the 16 lanes, then over the
+  // eight slots of each head
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    float x = nrm[g], y = vm[g];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-      y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
-    }
-    if ((r & 31) == 0) {
-      red[g][r >> 5] = x;
-      redv[g][r >> 5] = y;
-    }
+  for (int o = 8; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  if (c == 0) {
+    hk[r0] = nrm;
+    hv[r0] = vm;
   }
   __syncthreads();
-  if (r < 4) {
-    const float m = fmaxf(fmaxf(red[r][0], red[r][1]), fmaxf(red[r][2], red[r][3]));
+  if (threadIdx.x < kKVHeads) {
+    const int h = threadIdx.x;
+    float m = 0.f, mv = 0.f;
+    for (int q = h; q < kRowsPerPass; q += kKVHeads) {
+      m = fmaxf(m, hk[q]);
+      mv = fmaxf(mv, hv[q]);
+    }
     // Round up by a few ulps so the bound survives the rounding of the
     // tensor-core dot products.
-    kmax[int64_t(r) * p.nb_cap + gb] = m * 1.0001f;
-    vmax[int64_t(r) * p.nb_cap + gb] =
-        fmaxf(fmaxf(redv[r][0], redv[r][1]), fmaxf(redv[r][2], redv[r][3]));
+    kmax[int64_t(h) * p.nb_cap + gb] = m * 1.0001f;
+    vmax[int64_t(h) * p.nb_cap + gb] = mv;
   }
 }
 
 // ------------------------------------------------------------ fwd_v16
-// V as fp16 for the P.V products (P is fp16, and one tensor-core product
-// takes one operand type).  fp16 holds |v| up to 65504, so every value of
-// KV head g is scaled by 2^-e_g, e_g the smallest exponent that brings g's
-// largest |v| to at most 2^15 (0 for ordinary data, where the copy is exact);
-// the kernels multiply O by vscale[g] = 2^e_g.
+// V enters the P.V products as fp16 (P is fp16, and one tensor-core product
+// takes one operand type).  fp16 holds |v| up to 65504, so every value of KV
+// head g is scaled by 2^-e_g, e_g the smallest exponent that brings g's
+// largest |v| to at most 2^15 (0 for ordinary data); the kernels multiply O
+// by vscale[g] = 2^e_g.  fwd_kmax already wrote the unscaled copy, which is
+// exact and final when every e_g is 0; otherwise this kernel rewrites it.
 __device__ __forceinline__ float v_scale_in(float vmax) {
   if (!(vmax > 32768.f)) return 1.f;
   const int e = int(ceilf(log2f(vmax * (1.f / 32768.f))));
@@ -186,13 +203,16 @@ __global__ void __launch_bounds__(256) k_fwd_v16(msa_plan p, const __nv_bfloat16
   }
   __syncthreads();
   float sc[4];
+  bool scaled = false;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     float x = red[0][g];
     for (int k = 1; k < int(blockDim.x >> 5); ++k) x = fmaxf(x, red[k][g]);
     sc[g] = v_scale_in(x);
+    scaled |= sc[g] != 1.f;
   }
   if (blockIdx.x == 0 && threadIdx.x < 4) vscale[threadIdx.x] = 1.f / sc[threadIdx.x];
+  if (!scaled) return;
   const int64_t n = p.T * kKVHeads * kHeadDim / 8;  // 16-byte chunks, 16 per (token, head)
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
@@ -833,11 +853,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ------------------------------------------------------------ fwd_group
 // One item: octet A (and octet B) of one index head, whose tokens all see the
-// same blocks.  The CTA walks those blocks: per block S_A = Q_A K^T and
+// same blocks (uniform item), or which lie in a query block b small enough to
+// walk all of blocks 0 .. b with each token's rows masked to the blocks it
+// selected (dense item).  The CTA walks those blocks: per block S_A = Q_A K^T and
 // S_B = Q_B K^T, P = exp(s - m_ref) as fp16 over S's own first 64 columns,
 // then O_A += P_A V and O_B += P_B V, O accumulating in TMEM across the
-// blocks.  m_ref is a row's reference maximum, set from the item's first
-// block and raised only when a later block's maximum passes it by more than
+// blocks.  m_ref is a row's reference maximum, set from the first block the
+// row takes part in and raised only when a later block's maximum passes it by more than
 // 15 octaves (so P < 2^16 stays in fp16); then O and the row sum are
 // rescaled in place.  After the last block the softmax warps write their
 // octet's O = acc / l and LSE: no pool, no finalize, no shift bound.
@@ -1127,10 +1149,24 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const int32_t* it = items + item_index(i) * kItemWords;
         const ItemView iv = decode_item(it);
         const int32_t dstart = dinfo[iv.doc].start;
+        if (i + 1 < my_n) {
+          // the next item's Q tiles into L2: their loads then wait on L2,
+          // not on HBM, between this item's last S and the next item's first
+          const ItemView nv = decode_item(items + item_index(i + 1) * kItemWords);
+          for (int x = 0; x < (nv.tokB >= 0 ? 2 : 1); ++x) {
+            const int32_t t0 = x ? nv.tokB : nv.tokA;
+            const int nq = x ? nv.nqB : nv.nqA;
+            for (int qi = 0; qi < nq; ++qi) {
+              const int y = (t0 + qi) * kQHeads + nv.g * kHeadsPerGroup;
+              tma_prefetch_l2_2d(&mapQ, 0, y);
+              tma_prefetch_l2_2d(&mapQ, 64, y);
+            }
+          }
+        }
         // A's tile, K/V of the first block, B's tile, the other blocks
         ok = load_q(0, iv.tokA, iv.nqA, iv.g);
         for (int j = 0; ok && j < iv.nsel; ++j) {
-          ok = load_kv(iv.g, dstart + it[4 + j] * kBlock);
+          ok = load_kv(iv.g, dstart + (iv.dense ? j : it[4 + j]) * kBlock);
           if (ok && j == 0 && iv.tokB >= 0) ok = load_q(1, iv.tokB, iv.nqB, iv.g);
         }
       }
@@ -1164,11 +1200,13 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       const int nq = x ? iv.nqB : iv.nqA;
       const int32_t tok = tok0 + (qi < nq ? qi : nq - 1);
       const int32_t dstart = dinfo[iv.doc].start;
+      // dense item: the row's token takes part in block j where bit j is set
+      const uint32_t tmask = iv.dense ? uint32_t(it[4 + 8 * x + qi]) : ~0u;
       float mref = -INFINITY, lsum = 0.f;
       bool ok = true;
       for (int j = 0; j < iv.nsel; ++j) {
-        const int32_t key_start = dstart + it[4 + j] * kBlock;
-        const int jmax = qi < nq ? min(tok - key_start, kBlock - 1) : -1;
+        const int32_t key_start = dstart + (iv.dense ? j : it[4 + j]) * kBlock;
+        const int jmax = qi < nq && ((tmask >> j) & 1u) ? min(tok - key_start, kBlock - 1) : -1;
         // S_x(j) complete: so is P_x(j-1) . V, which was issued before it
         if (!mbar_wait_warp(smem_u32(&bars.s_full[x]), uint32_t(nx & 1), abort_flag)) {
           ok = false;
@@ -1407,9 +1445,9 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
 
   cudaError_t e;
   launch_begin("fwd_kmax", s);
-  k_fwd_kmax<<<unsigned(p.nb_cap), 128, 0, s>>>(p, static_cast<const __nv_bfloat16*>(k),
+  k_fwd_kmax<<<unsigned(p.nb_cap), kKmaxThreads, 0, s>>>(p, static_cast<const __nv_bfloat16*>(k),
                                                 static_cast<const __nv_bfloat16*>(v), kmax, vmax,
-                                                list);
+                                                list, v16);
   launch_end("fwd_kmax", s);
   launch_begin("fwd_v16", s);
   k_fwd_v16<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(

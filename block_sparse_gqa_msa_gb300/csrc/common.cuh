@@ -32,11 +32,13 @@ enum HeaderSlot {
   kHdrTriPerG = 6,  // count entries per index head
   kHdrItems = 7,    // octet-group items of the forward
   kHdrFTasks = 8,   // tasks of the forward's pooled task list
-  kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..32)
-  kHdrCostFill = 56,  // placement counters of the items, per cost
-  kHdrWords = 96
+  kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..64)
+  kHdrCostFill = 88,  // placement counters of the items, per cost
+  kHdrWords = 160
 };
-constexpr int kMaxItemCost = 2 * 16;  // an item: at most 2 octets x 16 blocks
+constexpr int kMaxDenseBlocks = 32;   // a dense octet's token masks are 32-bit words
+constexpr int kDefaultDenseBlocks = 28;
+constexpr int kMaxItemCost = 2 * kMaxDenseBlocks;  // an item: at most 2 octets x 32 blocks
 
 __device__ __forceinline__ void raise_status(int64_t* header, msa_status s) {
   atomicOr(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
@@ -77,13 +79,19 @@ __device__ __forceinline__ TaskView decode_task(int4 t) {
 
 // Octet-group item of the forward (int32 [kItemWords]): the tiles of one or
 // two aligned octets (8 consecutive tokens of a document, positions 8k ..
-// 8k+7, fewer at its end) whose tokens all see the same selected blocks.
+// 8k+7, fewer at its end) of one query block b.
 //   [0] first token of octet A, [1] first token of octet B (-1: none),
-//   [2] queries of A | queries of B << 4 | index head << 8 | blocks << 12,
-//   [3] document index, [4 .. 20) the blocks (document-local, ascending, -1).
+//   [2] queries of A | queries of B << 4 | index head << 8 | blocks << 12 |
+//       dense << 20,
+//   [3] document index,
+//   [4 .. 20) uniform item (all tokens see the same blocks): the blocks
+//       (document-local, ascending, -1 padded); dense item (blocks 0 .. b,
+//       b + 1 = the block count): per token of A then of B, the mask of the
+//       blocks it selected (bit v; 0 past the octet's end).
 constexpr int kItemWords = 20;
 struct ItemView {
   int32_t tokA, tokB, nqA, nqB, g, nsel, doc;
+  bool dense;
 };
 __device__ __forceinline__ ItemView decode_item(const int32_t* it) {
   const int4 h = *reinterpret_cast<const int4*>(it);
@@ -93,7 +101,8 @@ __device__ __forceinline__ ItemView decode_item(const int32_t* it) {
   v.nqA = h.z & 0xF;
   v.nqB = (h.z >> 4) & 0xF;
   v.g = (h.z >> 8) & 0x3;
-  v.nsel = (h.z >> 12) & 0x1F;
+  v.nsel = (h.z >> 12) & 0x3F;
+  v.dense = (h.z >> 20) & 1;
   v.doc = h.w;
   return v;
 }
@@ -137,7 +146,9 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
   L.task_cap = L.nnz_cap / kTaskQueries + L.tri_cap;
   // a document of n tokens has ceil(n / 8) <= n / 8 + 1 octets
   L.item_cap = int64_t(kKVHeads) * (T / 8 + D);
-  L.scan_tmp_len = ((L.tri_cap > L.task_cap ? L.tri_cap : L.task_cap) + 4095) / 4096 + 64;
+  // three scans' look-back status: per scan a ticket and one word per
+  // 4096-element tile, 64 bits each (in 32-bit units, a multiple of 6)
+  L.scan_tmp_len = 6 * (((L.tri_cap > L.task_cap ? L.tri_cap : L.task_cap) + 4095) / 4096 + 1);
   size_t o = 0;
   L.off_header = o;   o = align_up(o + sizeof(int64_t) * kHdrWords, 256);
   L.off_doc_info = o; o = align_up(o + sizeof(DocInfo) * D, 256);

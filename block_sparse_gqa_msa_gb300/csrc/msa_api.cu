@@ -235,7 +235,9 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   const int32_t Z = opts ? opts->super_block : 64;
   const int32_t acc = opts ? opts->dq_accum : MSA_DQ_ACCUM_F16;
   const int32_t oacc = opts ? opts->o_accum : MSA_O_ACCUM_F32;
+  const int32_t dense = opts ? opts->dense_blocks : 0;
   if (Z < 0 || acc < MSA_DQ_ACCUM_F16 || acc > MSA_DQ_ACCUM_F32) return MSA_ERR_INVALID_ARG;
+  if (dense < -1 || dense > kMaxDenseBlocks) return MSA_ERR_INVALID_ARG;
   if (oacc != MSA_O_ACCUM_F32 && oacc != MSA_O_ACCUM_BF16) return MSA_ERR_INVALID_ARG;
   // A bf16 O pool rounds every partial sum to 8 bits and O once more on the
   // store: up to one bf16 ulp of O (2^-6 for |O| in [2, 4)), above the 1e-2
@@ -254,6 +256,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   p.super_block = Z;
   p.dq_accum = acc;
   p.o_accum = oacc;
+  p.dense_blocks = dense == 0 ? kDefaultDenseBlocks : (dense < 0 ? 0 : dense);
   p.nb_cap = L.nb_cap;
   p.tri_cap = L.tri_cap;
   p.nnz_cap = L.nnz_cap;

@@ -27,6 +27,7 @@
 // block in shared memory: popcounts give the counts, prefix popcounts give
 // each query's rank, and duplicate slots collapse for free.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace msa {
 namespace {
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(1024) k_plan_docs(msa_plan p) {
     for (int i = 0; i < kHdrWords; ++i) hdr[i] = 0;
     bad = (offs[0] != 0 || int64_t(offs[D]) != p.T);
   }
+  for (int64_t i = threadIdx.x; i < p.scan_tmp_len; i += blockDim.x) p.scan_tmp[i] = 0;
   __syncthreads();
   for (int d = threadIdx.x; d < D; d += blockDim.x)
     if (offs[d + 1] <= offs[d]) bad = 1;
@@ -131,6 +133,8 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
   __shared__ unsigned long long s_pairs;
   __shared__ int s_nsel[16];        // per octet: blocks selected by any of its queries
   __shared__ uint32_t s_bad, s_pdiff;  // octets not uniform; pairs with different sets
+  __shared__ uint32_t s_mask[128];     // dense octets: each query's block mask
+  __shared__ int64_t s_hist[kMaxItemCost + 1];  // items per cost
   int64_t* hdr = p.header;
   const int64_t NB = hdr[kHdrNB];
   const int g = int(blockIdx.x / p.nb_cap);
@@ -231,15 +235,22 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
       }
     } else if (PASS == kPassScatter) {
       if (valid) {
+        // all bucket offsets in flight before the first use
+        int32_t dst[kTopK];
+#pragma unroll
+        for (int i = 0; i < kTopK; ++i) {
+          const int64_t v = sl[i];
+          dst[i] = (v >= c0 && v <= cend) ? p.off[seg + tri_local(n, Zs, v, qb)] : 0;
+        }
+        const int w = r >> 5;
 #pragma unroll
         for (int i = 0; i < kTopK; ++i) {
           const int64_t v = sl[i];
           if (v < c0 || v > cend) continue;
           const uint32_t* b = bm[v - c0];
-          const int w = r >> 5;
           int rank = __popc(b[w] & ((1u << (r & 31)) - 1u));
           for (int k = 0; k < w; ++k) rank += __popc(b[k]);
-          p.col[p.off[seg + tri_local(n, Zs, v, qb)] + rank] = int32_t(t);
+          p.col[dst[i] + rank] = int32_t(t);
           pairs += (v < qb) ? kBlock : (pos - qb * kBlock + 1);
         }
       }
@@ -279,9 +290,13 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
           task.w = int32_t(int64_t(g) * p.nb_cap + di.blk_base + v);
           reinterpret_cast<int4*>(p.tasks)[p.toff[e] + i] = task;
           // the forward's pooled list keeps tasks with an ungrouped query
+          int32_t tq[kTaskQueries];
+#pragma unroll
+          for (int k = 0; k < kTaskQueries; ++k) tq[k] = k < nq ? p.col[task.x + k] : -1;
           int keep = 0;
-          for (int k = 0; k < nq; ++k)
-            keep |= p.grouped[int64_t(g) * p.T + p.col[task.x + k]] == 0;
+#pragma unroll
+          for (int k = 0; k < kTaskQueries; ++k)
+            keep |= tq[k] >= 0 && p.grouped[int64_t(g) * p.T + tq[k]] == 0;
           p.fflag[p.toff[e] + i] = keep;
         }
       }
@@ -292,45 +307,74 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
     if (my_nsel) atomicAdd(&s_nsel[oct], my_nsel);
     if (my_bad) atomicOr(&s_bad, 1u << oct);
     if (my_pdiff) atomicOr(&s_pdiff, 1u << (oct >> 1));
+    // dense octets: this query's visible selected blocks as a bit mask
+    const bool dense_ok = qb + 1 <= p.dense_blocks;
+    // items per cost (complete after the count pass), for the placements
+    if (PASS == kPassScatter && threadIdx.x <= kMaxItemCost)
+      s_hist[threadIdx.x] = threadIdx.x == 0 ? 0 : hdr[kHdrCost + threadIdx.x];
+    if (PASS == kPassScatter && dense_ok) {
+      uint32_t m = 0u;
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i)
+        if (sl[i] >= 0 && sl[i] <= qb) m |= 1u << sl[i];
+      s_mask[r] = m;
+    }
     __syncthreads();
+    // s_nsel[o]: blocks some query of octet o selected; s_bad bit o: some
+    // block selected by only part of its queries
     auto uniform = [&](int o) {
       return octet_rows(o) > 0 && s_nsel[o] > 0 && !((s_bad >> o) & 1u);
     };
-    auto paired = [&](int i) {
-      return uniform(2 * i) && uniform(2 * i + 1) && !((s_pdiff >> i) & 1u);
+    auto dense = [&](int o) {
+      return dense_ok && octet_rows(o) > 0 && s_nsel[o] > 0 && ((s_bad >> o) & 1u);
     };
-    if (PASS == kPassCount && valid)
-      p.grouped[int64_t(g) * p.T + t] = uniform(r >> 3) ? 1 : 0;
+    auto paired = [&](int i) {
+      return (uniform(2 * i) && uniform(2 * i + 1) && !((s_pdiff >> i) & 1u)) ||
+             (dense(2 * i) && dense(2 * i + 1));
+    };
     const int o = r >> 3;
-    if ((r & 7) == 0 && uniform(o) && !((o & 1) && paired(o >> 1))) {
+    if (PASS == kPassCount && valid)
+      p.grouped[int64_t(g) * p.T + t] = (uniform(o) || dense(o)) ? 1 : 0;
+    const bool dn = dense(o);
+    if ((r & 7) == 0 && (uniform(o) || dn) && !((o & 1) && paired(o >> 1))) {
       const bool hasB = !(o & 1) && paired(o >> 1);
-      const int cost = s_nsel[o] * (hasB ? 2 : 1);
+      const int nsel = dn ? int(qb) + 1 : s_nsel[o];
+      const int cost = nsel * (hasB ? 2 : 1);
       unsigned long long* cnt = reinterpret_cast<unsigned long long*>(hdr + kHdrCost);
       if (PASS == kPassCount) {
         atomicAdd(cnt + cost, 1ull);
       } else {
         int64_t pos = 0;  // items of higher cost come first
-        for (int c = cost + 1; c <= kMaxItemCost; ++c) pos += hdr[kHdrCost + c];
+        for (int c = cost + 1; c <= kMaxItemCost; ++c) pos += s_hist[c];
         pos += int64_t(atomicAdd(
             reinterpret_cast<unsigned long long*>(hdr + kHdrCostFill) + cost, 1ull));
         int32_t* it = p.items + pos * kItemWords;
         *reinterpret_cast<int4*>(it) =
             make_int4(int32_t(t), hasB ? int32_t(t + 8) : -1,
                       octet_rows(o) | (hasB ? octet_rows(o + 1) : 0) << 4 | g << 8 |
-                          s_nsel[o] << 12,
+                          nsel << 12 | (dn ? 1 : 0) << 20,
                       d);
-        // this query's visible blocks (distinct after the dedupe), ascending
-        int nb = 0;
+        if (dn) {
+          // the masks of the queries of A, then of B (0 past an octet's end)
 #pragma unroll
-        for (int i = 0; i < kTopK; ++i) {
-          if (sl[i] < 0 || sl[i] > qb) continue;
-          int rank = 0;
+          for (int k = 0; k < 16; ++k) {
+            const int oo = o + (k >> 3), qi = k & 7;
+            it[4 + k] = (k < 8 || hasB) && qi < octet_rows(oo) ? int32_t(s_mask[8 * oo + qi]) : 0;
+          }
+        } else {
+          // this query's visible blocks (distinct after the dedupe), ascending
+          int nb = 0;
 #pragma unroll
-          for (int j = 0; j < kTopK; ++j) rank += (sl[j] >= 0 && sl[j] < sl[i]);
-          it[4 + rank] = sl[i];
-          ++nb;
+          for (int i = 0; i < kTopK; ++i) {
+            if (sl[i] < 0 || sl[i] > qb) continue;
+            int rank = 0;
+#pragma unroll
+            for (int j = 0; j < kTopK; ++j) rank += (sl[j] >= 0 && sl[j] < sl[i]);
+            it[4 + rank] = sl[i];
+            ++nb;
+          }
+          for (int k = nb; k < kTopK; ++k) it[4 + k] = -1;
         }
-        for (int k = nb; k < kTopK; ++k) it[4 + k] = -1;
       }
     }
     if (PASS == kPassScatter && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -349,48 +393,41 @@ __global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
 }
 
 // ------------------------------------------------------------ device scan
-// Exclusive scan of in[0, n) -> out, n read from the device; the total goes to
-// *total.  Three launches, grids sized by capacity.
-__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(const int32_t* in, const int64_t* n_ptr,
-                                                              int32_t* sums) {
-  __shared__ int64_t tot;
-  const int64_t n = *n_ptr;
-  const int64_t base = int64_t(blockIdx.x) * kScanTile;
-  if (base >= n) return;
-  int64_t s = 0;
-#pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    const int64_t j = base + int64_t(threadIdx.x) * kScanItems + i;
-    if (j < n) s += in[j];
-  }
-  block_excl_scan<int64_t>(s, &tot);
-  if (threadIdx.x == 0) sums[blockIdx.x] = int32_t(tot);
-}
+// Exclusive scan of in[0, n) -> out in one pass, n read from the device; the
+// total goes to *total.  Decoupled look-back (Merrill and Garland,
+// "Single-pass Parallel Prefix Scan with Decoupled Look-back", 2016): a CTA
+// takes the next tile by ticket, publishes the tile's sum, then adds up the
+// published sums of the tiles before it, back to the first tile that has
+// published its inclusive prefix, and publishes its own.  Tickets go out in
+// the order CTAs start, so a CTA only waits on CTAs that already run; the
+// wait is bounded all the same (MSA_ERR_TIMEOUT, and the CTA publishes
+// anyway so that later tiles finish).  st[0] is the ticket counter and
+// st[1 + j] the status of tile j: zero, or a flag in the top two bits above
+// the value.  k_plan_docs zeroes them.  With a compaction target, element j's
+// record csrc[j] is also copied to cdst[out[j]] where in[j] != 0.
+constexpr unsigned long long kStAgg = 1ull << 62;   // tile sum published
+constexpr unsigned long long kStPre = 1ull << 63;   // inclusive prefix published
+constexpr unsigned long long kStVal = kStAgg - 1;
 
-__global__ void __launch_bounds__(kScanThreads) k_scan_sums(int32_t* sums, const int64_t* n_ptr,
-                                                            int64_t* total) {
-  __shared__ int64_t tot;
-  const int64_t n = *n_ptr;
-  const int64_t nb = (n + kScanTile - 1) / kScanTile;
-  int64_t carry = 0;
-  for (int64_t base = 0; base < nb; base += blockDim.x) {
-    const int64_t j = base + threadIdx.x;
-    const int64_t x = j < nb ? sums[j] : 0;
-    const int64_t ex = block_excl_scan<int64_t>(x, &tot);
-    if (j < nb) sums[j] = int32_t(carry + ex);
-    carry += tot;
-    __syncthreads();
+__global__ void __launch_bounds__(kScanThreads) k_scan(const int32_t* in, int32_t* out,
+                                                       const int64_t* n_ptr, int64_t cap,
+                                                       int64_t* total, unsigned long long* st,
+                                                       int64_t* hdr, const int4* csrc,
+                                                       int4* cdst) {
+  __shared__ int64_t tot, excl_sh;
+  __shared__ unsigned tile_sh;
+  // A failed plan's counts are not to be trusted (an earlier pass stopped
+  // early): nothing to scan then.  n never exceeds the arrays' capacity.
+  const int64_t n_dev = plan_failed(hdr) ? 0 : *n_ptr;
+  const int64_t n = n_dev < 0 ? 0 : (n_dev > cap ? cap : n_dev);
+  if (threadIdx.x == 0) tile_sh = atomicAdd(reinterpret_cast<unsigned*>(st), 1u);
+  __syncthreads();
+  const int64_t tile = tile_sh;
+  const int64_t base = tile * kScanTile;
+  if (base >= n) {
+    if (tile == 0 && threadIdx.x == 0) *total = 0;
+    return;
   }
-  if (threadIdx.x == 0) *total = carry;
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan_down(const int32_t* in, int32_t* out,
-                                                            const int64_t* n_ptr,
-                                                            const int32_t* sums) {
-  __shared__ int64_t tot;
-  const int64_t n = *n_ptr;
-  const int64_t base = int64_t(blockIdx.x) * kScanTile;
-  if (base >= n) return;
   int32_t v[kScanItems];
   int64_t s = 0;
 #pragma unroll
@@ -399,32 +436,74 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_down(const int32_t* in, i
     v[i] = j < n ? in[j] : 0;
     s += v[i];
   }
-  int64_t run = block_excl_scan<int64_t>(s, &tot) + sums[blockIdx.x];
+  const int64_t ex = block_excl_scan<int64_t>(s, &tot);
+  if (threadIdx.x < 32) {
+    // warp 0 looks back over windows of 32 predecessors at a time
+    const int lane = threadIdx.x;
+    volatile unsigned long long* stv = st + 1;
+    int64_t prefix = 0;
+    if (tile > 0) {
+      if (lane == 0) stv[tile] = kStAgg | (unsigned long long)tot;
+      const uint64_t t0 = global_timer_ns();
+      for (int64_t top = tile - 1;;) {
+        const int64_t k = top - lane;
+        // (before tile 0: an inclusive prefix of 0)
+        const unsigned long long x =
+            k >= 0 ? (unsigned long long)stv[k] : (unsigned long long)kStPre;
+        const unsigned ready = __ballot_sync(0xffffffffu, x != 0ull);
+        const unsigned pre = __ballot_sync(0xffffffffu, (x & kStPre) != 0ull);
+        // lanes up to the nearest inclusive prefix, when all of them are in
+        const unsigned need = pre ? (pre & (0u - pre)) * 2u - 1u : 0xffffffffu;
+        if ((ready & need) == need) {
+          int64_t val = (need >> lane) & 1u ? int64_t(x & kStVal) : 0;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xffffffffu, val, o);
+          prefix += val;
+          if (pre) break;
+          top -= 32;
+          continue;
+        }
+        const bool late = __shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitTimeoutNs, 0);
+        if (late) {
+          if (lane == 0) raise_status(hdr, MSA_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    if (lane == 0) {
+      stv[tile] = kStPre | (unsigned long long)(prefix + tot);
+      excl_sh = prefix;
+      if (base + kScanTile >= n) *total = prefix + tot;
+    }
+  }
+  __syncthreads();
+  int64_t run = excl_sh + ex;
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
     const int64_t j = base + int64_t(threadIdx.x) * kScanItems + i;
-    if (j < n) out[j] = int32_t(run);
+    if (j < n) {
+      out[j] = int32_t(run);
+      if (cdst != nullptr && v[i] != 0) cdst[run] = csrc[j];
+    }
     run += v[i];
   }
 }
 
-// The forward's pooled task list: tasks with fflag set, in task order.
-__global__ void __launch_bounds__(256) k_ftask_scatter(msa_plan p) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (plan_failed(p.header) || i >= p.header[kHdrTasks]) return;
-  if (p.fflag[i])
-    reinterpret_cast<int4*>(p.ftasks)[p.fpos[i]] = reinterpret_cast<const int4*>(p.tasks)[i];
+// scan k of the plan (0: cnt, 1: tcnt, 2: fflag) uses status region k
+__host__ __device__ inline unsigned long long* scan_status(const msa_plan& p, int k) {
+  const int64_t region = p.scan_tmp_len / 6;  // (tiles + 1) words of 64 bits each
+  return reinterpret_cast<unsigned long long*>(p.scan_tmp) + k * region;
 }
 
-cudaError_t scan(const int32_t* in, int32_t* out, const int64_t* n_ptr, int64_t cap,
-                 int32_t* tmp, int64_t* total, cudaStream_t s) {
+cudaError_t scan(const msa_plan& p, int k, const int32_t* in, int32_t* out, const int64_t* n_ptr,
+                 int64_t cap, int64_t* total, cudaStream_t s, const int4* csrc = nullptr,
+                 int4* cdst = nullptr) {
   const unsigned grid = unsigned((cap + kScanTile - 1) / kScanTile);
   if (grid == 0) return cudaSuccess;
-  launch_begin("plan_scan", s);
-  k_scan_reduce<<<grid, kScanThreads, 0, s>>>(in, n_ptr, tmp);
-  k_scan_sums<<<1, kScanThreads, 0, s>>>(tmp, n_ptr, total);
-  k_scan_down<<<grid, kScanThreads, 0, s>>>(in, out, n_ptr, tmp);
-  launch_end("plan_scan", s, 3);
+  launch_begin(k == 2 ? "plan_ftasks" : "plan_scan", s);
+  k_scan<<<grid, kScanThreads, 0, s>>>(in, out, n_ptr, cap, total, scan_status(p, k), p.header,
+                                       csrc, cdst);
+  launch_end(k == 2 ? "plan_ftasks" : "plan_scan", s);
   return cudaGetLastError();
 }
 
@@ -438,24 +517,19 @@ cudaError_t launch_plan(const msa_plan& p, cudaStream_t s) {
   launch_begin("plan_count", s);
   k_plan_blocks<kPassCount><<<grid, 128, 0, s>>>(p);
   launch_end("plan_count", s);
-  cudaError_t e = scan(p.cnt, p.off, p.header + kHdrTri, p.tri_cap, p.scan_tmp,
-                       p.header + kHdrNnz, s);
+  cudaError_t e = scan(p, 0, p.cnt, p.off, p.header + kHdrTri, p.tri_cap, p.header + kHdrNnz, s);
   if (e != cudaSuccess) return e;
   launch_begin("plan_scatter", s);
   k_plan_blocks<kPassScatter><<<grid, 128, 0, s>>>(p);
   launch_end("plan_scatter", s);
-  e = scan(p.tcnt, p.toff, p.header + kHdrTri, p.tri_cap, p.scan_tmp, p.header + kHdrTasks, s);
+  e = scan(p, 1, p.tcnt, p.toff, p.header + kHdrTri, p.tri_cap, p.header + kHdrTasks, s);
   if (e != cudaSuccess) return e;
   launch_begin("plan_emit", s);
   k_plan_blocks<kPassEmit><<<grid, 128, 0, s>>>(p);
   launch_end("plan_emit", s);
-  e = scan(p.fflag, p.fpos, p.header + kHdrTasks, p.task_cap, p.scan_tmp,
-           p.header + kHdrFTasks, s);
-  if (e != cudaSuccess) return e;
-  launch_begin("plan_ftasks", s);
-  k_ftask_scatter<<<unsigned((p.task_cap + 255) / 256), 256, 0, s>>>(p);
-  launch_end("plan_ftasks", s);
-  return cudaGetLastError();
+  // the forward's pooled list: tasks with fflag set, in task order
+  return scan(p, 2, p.fflag, p.fpos, p.header + kHdrTasks, p.task_cap, p.header + kHdrFTasks, s,
+              reinterpret_cast<const int4*>(p.tasks), reinterpret_cast<int4*>(p.ftasks));
 }
 
 }  // namespace msa

@@ -126,6 +126,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// L2 prefetch of one box (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Bulk tensor reduction: global tile (+)= shared tile (dense box layout of
 // the tensor map; element type and add semantics from the map).
 __device__ __forceinline__ void tma_reduce_add_2d(const void* map, uint32_t src, int x, int y) {

@@ -105,7 +105,14 @@ typedef struct msa_plan_options {
   int32_t dq_accum;
   /* An msa_o_accum value; only (0) MSA_O_ACCUM_F32 is accepted. */
   int32_t o_accum;
-  int32_t reserved[5];
+  /* Dense octets of the forward: an aligned run of 8 tokens in query block
+   * b whose tokens see different blocks runs as one tile over all blocks
+   * 0 .. b, each token's rows masked to its own blocks, when b + 1 <=
+   * dense_blocks (instead of through the pooled tasks).  0 selects the
+   * default, 28; -1 turns dense octets off; 1 .. 32 set the bound; other
+   * values give MSA_ERR_INVALID_ARG. */
+  int32_t dense_blocks;
+  int32_t reserved[4];
 } msa_plan_options;
 
 /*
@@ -129,6 +136,7 @@ typedef struct msa_plan {
   int32_t super_block;
   int32_t dq_accum;
   int32_t o_accum;
+  int32_t dense_blocks; /* the bound in effect (0: no dense octets)     */
   int64_t nb_cap;     /* bound on the number of 128-key blocks            */
   int64_t tri_cap;    /* bound on (index head, doc, key block, query block) */
   int64_t nnz_cap;    /* bound on CSR entries                              */

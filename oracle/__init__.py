@@ -90,7 +90,7 @@ def _bind(lib):
     lib.oracle_select_blocks.argtypes = [_P, _P, _I64, _I32, _P, _I32, _I32, _P]
     lib.oracle_select_blocks.restype = ctypes.c_int
     lib.oracle_block_scores.argtypes = [_P, _P, _I64, _I32, _P, _I32, _P, _I64, _I64, _P]
-    lib.oracle_groups.argtypes = [_P, _I64, _P, _I32, _P, _P, _I64, _P]
+    lib.oracle_groups.argtypes = [_P, _I64, _P, _I32, _I32, _P, _P, _I64, _P]
     lib.oracle_groups.restype = ctypes.c_int
     lib.oracle_block_scores.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
@@ -246,20 +246,25 @@ def plan(q2k, doc_offsets, T: int, super_block: int = 16, lib=None):
     }
 
 
-def groups(q2k, doc_offsets, T: int, lib=None):
+DENSE_BLOCKS = 28
+
+
+def groups(q2k, doc_offsets, T: int, dense_blocks: int = DENSE_BLOCKS, lib=None):
     """Octet groups of the forward schedule (see oracle_groups in
-    msa_oracle.c): {"grouped": uint8 [4, T], "items": int64 [n, 22]} with item
-    rows (tokA, tokB or -1, nqA, nqB, g, nsel, 16 blocks ascending, -1 padded)."""
+    msa_oracle.c): {"grouped": uint8 [4, T], "items": int64 [n, 23]} with item
+    rows (tokA, tokB or -1, nqA, nqB, g, nsel, dense, then 16 blocks
+    ascending and -1 padded for a uniform item, or the 16 tokens' block
+    masks for a dense one).  dense_blocks <= 0: no dense octets."""
     lib = lib or _load()
     q2k = _i32(q2k)
     offs = _i32(doc_offsets)
     D = offs.size - 1
     grouped = np.zeros((4, T), dtype=np.uint8)
     cap = 4 * (T // 8 + D) + 4
-    items = np.zeros((cap, 22), dtype=np.int64)
+    items = np.zeros((cap, 23), dtype=np.int64)
     counts = np.zeros(1, dtype=np.int64)
-    rc = lib.oracle_groups(_ptr(q2k), T, _ptr(offs), D, _ptr(grouped), _ptr(items), cap,
-                           _ptr(counts))
+    rc = lib.oracle_groups(_ptr(q2k), T, _ptr(offs), D, int(dense_blocks), _ptr(grouped),
+                           _ptr(items), cap, _ptr(counts))
     _check(rc, "groups")
     return {"grouped": grouped, "items": items[:int(counts[0])].copy()}
 

@@ -523,23 +523,36 @@ int oracle_threads(void) {
  * of one query set are merged).
  *
  * For index head g, the tokens of document d are cut into aligned octets:
- * document positions 8k .. 8k+7 (fewer at the document's end).  An octet is
- * GROUPED when all its tokens have the same non-empty set of visible
- * selected blocks {v in q2k[g, t, :] : 0 <= v <= own block} (all tokens of an
- * octet share their block).  A grouped octet's rows see exactly its blocks,
- * so one tile can accumulate them block after block without a merge.
- * Grouped octets at positions 16k and 16k+8 of one document with the same
- * set form one item; every other grouped octet is an item alone.
+ * document positions 8k .. 8k+7 (fewer at the document's end), all in one
+ * block b.  S_t = {v in q2k[g, t, :] : 0 <= v <= b} is token t's set of
+ * visible selected blocks.  An octet is
+ *   UNIFORM when all its tokens have the same non-empty S_t: its tile walks
+ *     exactly those blocks;
+ *   DENSE when it is not uniform, b + 1 <= dense_blocks and some S_t is
+ *     non-empty: its tile walks all blocks 0 .. b, and a token's rows take
+ *     part in block v only where v is in S_t (a per-token bit mask);
+ * and GROUPED when it is either: one tile then accumulates its rows block
+ * after block without a merge.  Octets 2i and 2i+1 of a document form one
+ * item when both are uniform with the same set, or both dense (the same
+ * blocks 0 .. b); every other grouped octet is an item alone.
  *   grouped: uint8 [4][T]  (1 = the token's octet is grouped)
- *   items:   int64 [cap][6 + 16]: tokA, tokB (-1 if none), nqA, nqB, g,
- *            nsel, blocks ascending (-1 padded); items in (g, d, k) order
+ *   items:   int64 [cap][23]: tokA, tokB (-1 if none), nqA, nqB, g, nsel,
+ *            dense, then 16 words: uniform - the blocks ascending (-1
+ *            padded); dense - the masks (bit v = v in S_t) of tokens
+ *            tokA .. tokA+7 and tokB .. tokB+7 (0 past the octet's end);
+ *            nsel = |S| (uniform) or b + 1 (dense); items in (g, d, k) order
  *   counts:  [0] = items
- * The forward's task list is then the task list without the tasks all of
- * whose queries are grouped (see oracle/__init__.py).
+ * dense_blocks <= 0 makes no octet dense; it is at most 32 (one 32-bit mask
+ * per token).  The forward's task list is then the task list without the
+ * tasks all of whose queries are grouped (see oracle/__init__.py).
  */
+#define ITEM_WORDS 23
+enum { OCT_NONE = 0, OCT_UNIFORM = 1, OCT_DENSE = 2 };
+
 int oracle_groups(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D,
-                  unsigned char* grouped, int64_t* items, int64_t item_cap, int64_t* counts) {
-  if (T <= 0 || check_offsets(offs, D, T)) return OR_BAD_ARGS;
+                  int32_t dense_blocks, unsigned char* grouped, int64_t* items,
+                  int64_t item_cap, int64_t* counts) {
+  if (T <= 0 || check_offsets(offs, D, T) || dense_blocks > 32) return OR_BAD_ARGS;
   if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
   int32_t maxnb = 0;
   for (int32_t d = 0; d < D; ++d)
@@ -556,64 +569,88 @@ int oracle_groups(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D,
       const int32_t nb = nblocks(len);
       /* octet k covers document positions [8k, min(8k + 8, len)) */
       const int32_t noct = (len + 7) / 8;
-      int32_t* oct_nsel = (int32_t*)malloc(sizeof(int32_t) * (size_t)noct);
+      int* kind = (int*)malloc(sizeof(int) * (size_t)noct);
       for (int32_t k = 0; k < noct; ++k) {
         const int64_t t0 = st + 8 * (int64_t)k;
         const int64_t t1 = (8 * (int64_t)k + 8 < len) ? t0 + 8 : st + len;
         const int32_t b = (int32_t)(8 * (int64_t)k / BLK);
+        int same = 1, any = 0;
         selection(q2k, T, g, t0, nb, s0);
-        int32_t nsel = 0;
-        for (int32_t v = 0; v <= b; ++v) nsel += s0[v];
-        int same = nsel > 0;
-        for (int64_t t = t0 + 1; t < t1 && same; ++t) {
+        for (int32_t v = 0; v <= b; ++v) any |= s0[v];
+        const int first_nonempty = any;
+        for (int64_t t = t0 + 1; t < t1; ++t) {
           selection(q2k, T, g, t, nb, s1);
-          for (int32_t v = 0; v <= b; ++v)
+          for (int32_t v = 0; v <= b; ++v) {
+            any |= s1[v];
             if (s1[v] != s0[v]) same = 0;
+          }
         }
-        oct_nsel[k] = same ? nsel : 0;
-        if (same)
+        if (same && first_nonempty)
+          kind[k] = OCT_UNIFORM;
+        else if (!same && any && b + 1 <= dense_blocks)
+          kind[k] = OCT_DENSE;
+        else
+          kind[k] = OCT_NONE;
+        if (kind[k] != OCT_NONE)
           for (int64_t t = t0; t < t1; ++t) grouped[(int64_t)g * T + t] = 1;
       }
-      for (int32_t k = 0; k < noct && !rc; ++k) {
-        if (!oct_nsel[k]) continue;
-        const int64_t t0 = st + 8 * (int64_t)k;
+      /* octets k, k+1 (k even) pair when both dense, or both uniform with
+         the same set */
+      int* paired = (int*)calloc((size_t)noct, sizeof(int));
+      for (int32_t k = 0; k + 1 < noct; k += 2) {
         const int32_t b = (int32_t)(8 * (int64_t)k / BLK);
-        int pair = 0;
-        if (k % 2 == 0 && k + 1 < noct && oct_nsel[k + 1]) {
-          selection(q2k, T, g, t0, nb, s0);
-          selection(q2k, T, g, t0 + 8, nb, s1);
-          pair = 1;
+        if (kind[k] == OCT_DENSE && kind[k + 1] == OCT_DENSE) {
+          paired[k] = 1;
+        } else if (kind[k] == OCT_UNIFORM && kind[k + 1] == OCT_UNIFORM) {
+          selection(q2k, T, g, st + 8 * (int64_t)k, nb, s0);
+          selection(q2k, T, g, st + 8 * (int64_t)k + 8, nb, s1);
+          paired[k] = 1;
           for (int32_t v = 0; v <= b; ++v)
-            if (s0[v] != s1[v]) pair = 0;
+            if (s0[v] != s1[v]) paired[k] = 0;
         }
-        if (k % 2 == 1 && oct_nsel[k - 1]) { /* partner of an even octet? */
-          selection(q2k, T, g, t0 - 8, nb, s0);
-          selection(q2k, T, g, t0, nb, s1);
-          int same = 1;
-          for (int32_t v = 0; v <= b; ++v)
-            if (s0[v] != s1[v]) same = 0;
-          if (same) continue; /* already in the even octet's item */
-        }
+      }
+      for (int32_t k = 0; k < noct && !rc; ++k) {
+        if (kind[k] == OCT_NONE || (k % 2 == 1 && paired[k - 1])) continue;
         if (n >= item_cap) {
           rc = OR_CAPACITY;
           break;
         }
-        int64_t* it = items + n * 22;
+        const int pair = k % 2 == 0 && paired[k];
+        const int64_t t0 = st + 8 * (int64_t)k;
+        const int32_t b = (int32_t)(8 * (int64_t)k / BLK);
+        int64_t* it = items + n * ITEM_WORDS;
         const int32_t nqa = (8 * k + 8 < len) ? 8 : len - 8 * k;
+        const int32_t nqb = pair ? ((8 * (k + 1) + 8 < len) ? 8 : len - 8 * (k + 1)) : 0;
         it[0] = t0;
         it[1] = pair ? t0 + 8 : -1;
         it[2] = nqa;
-        it[3] = pair ? ((8 * (k + 1) + 8 < len) ? 8 : len - 8 * (k + 1)) : 0;
+        it[3] = nqb;
         it[4] = g;
-        it[5] = oct_nsel[k];
-        selection(q2k, T, g, t0, nb, s0);
-        int32_t j = 0;
-        for (int32_t v = 0; v <= b; ++v)
-          if (s0[v]) it[6 + j++] = v;
-        for (; j < TOPK; ++j) it[6 + j] = -1;
+        it[6] = kind[k] == OCT_DENSE;
+        if (kind[k] == OCT_UNIFORM) {
+          selection(q2k, T, g, t0, nb, s0);
+          int32_t j = 0;
+          for (int32_t v = 0; v <= b; ++v)
+            if (s0[v]) it[7 + j++] = v;
+          it[5] = j;
+          for (; j < TOPK; ++j) it[7 + j] = -1;
+        } else {
+          it[5] = b + 1;
+          for (int x = 0; x < 2; ++x)
+            for (int i = 0; i < 8; ++i) {
+              int64_t mask = 0;
+              if (i < (x ? nqb : nqa)) {
+                selection(q2k, T, g, t0 + 8 * x + i, nb, s0);
+                for (int32_t v = 0; v <= b; ++v)
+                  if (s0[v]) mask |= (int64_t)1 << v;
+              }
+              it[7 + 8 * x + i] = mask;
+            }
+        }
         ++n;
       }
-      free(oct_nsel);
+      free(kind);
+      free(paired);
     }
   counts[0] = n;
   free(s0);

@@ -69,17 +69,22 @@ def canonical_oracle_plan(pl):
     return buckets, tasks
 
 
-def canonical_items(items, blocks_at):
-    """Octet-group items -> sorted [(g, tokA, tokB, nqA, nqB, nsel, blocks...)].
-    GPU rows: tokA, tokB, nqA | nqB << 4 | g << 8 | nsel << 12, doc, blocks
-    (blocks_at=4); oracle rows: tokA, tokB, nqA, nqB, g, nsel, blocks (6)."""
+def canonical_items(items, gpu):
+    """Octet-group items -> sorted [(g, tokA, tokB, nqA, nqB, nsel, dense,
+    16 words: blocks or masks)].  GPU rows (gpu=True): tokA, tokB,
+    nqA | nqB << 4 | g << 8 | nsel << 12 | dense << 20, doc, 16 words; oracle
+    rows: tokA, tokB, nqA, nqB, g, nsel, dense, 16 words."""
     out = []
     for r in items:
         r = [int(x) for x in r]
-        if blocks_at == 4:
+        if gpu:
             z = r[2]
-            key = (z >> 8 & 3, r[0], r[1], z & 0xF, z >> 4 & 0xF, z >> 12 & 0x1F)
+            key = (z >> 8 & 3, r[0], r[1], z & 0xF, z >> 4 & 0xF, z >> 12 & 0x3F, z >> 20 & 1)
+            words = r[4:20]
         else:
-            key = (r[4], r[0], r[1], r[2], r[3], r[5])
-        out.append(key + tuple(r[blocks_at:blocks_at + 16]))
+            key = (r[4], r[0], r[1], r[2], r[3], r[5], r[6])
+            words = r[7:23]
+        if key[6]:  # dense: 32-bit masks, unsigned
+            words = [w & 0xFFFFFFFF for w in words]
+        out.append(key + tuple(words))
     return sorted(out)

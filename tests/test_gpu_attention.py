@@ -56,10 +56,10 @@ def oracle_results(name):
     return w, O, L, dQ, dK, dV
 
 
-def run_gpu(w, super_block=16, dq_accum="f16", status=0):
+def run_gpu(w, super_block=16, dq_accum="f16", status=0, dense_blocks=0):
     q, k, v, do = (x.to(DEV) for x in (w.q, w.k, w.v, w.do))
     plan = api.msa_build_plan(w.q2k.to(DEV), w.doc_offsets.to(DEV), super_block=super_block,
-                              dq_accum=dq_accum)
+                              dq_accum=dq_accum, dense_blocks=dense_blocks)
     o, lse = api.msa_forward(plan, q, k, v, w.scale)
     dq, dk, dv = api.msa_backward(plan, q, k, v, o, lse, do, w.scale)
     torch.cuda.synchronize()
@@ -67,10 +67,14 @@ def run_gpu(w, super_block=16, dq_accum="f16", status=0):
     return tuple(x.float().cpu().numpy() for x in (o, lse, dq, dk, dv))
 
 
+# dense_blocks: the default (these documents' octets then all run in the
+# group kernel), off (the pooled kernel takes every non-uniform octet), and a
+# bound of 3 blocks (both schedules in one call)
+@pytest.mark.parametrize("dense", [0, -1, 3])
 @pytest.mark.parametrize("name", list(CASES))
-def test_forward_matches_oracle(name):
+def test_forward_matches_oracle(name, dense):
     w, O, L, *_ = oracle_results(name)
-    o, lse, *_ = run_gpu(w)
+    o, lse, *_ = run_gpu(w, dense_blocks=dense)
     check_o(o, O)
     check_lse(lse, L)
 

@@ -32,11 +32,11 @@ STRUCTURES = {
 }
 
 
-def _check(lens, q2k, Z):
+def _check(lens, q2k, Z, dense=0):
     offs = inputs.offsets_from_lengths(lens)
     T = int(sum(lens))
     plan = api.msa_build_plan(torch.from_numpy(q2k).to(DEV), torch.from_numpy(offs).to(DEV),
-                              super_block=Z)
+                              super_block=Z, dense_blocks=dense)
     assert api.msa_read_status(plan) == 0
     counts = api.msa_plan_counts(plan)
     col, tasks = api.msa_plan_export(plan)
@@ -57,11 +57,12 @@ def _check(lens, q2k, Z):
     assert counts["pairs"] == n
     # the forward's octet groups
     grouped, items, ftasks = api.msa_plan_export_groups(plan)
-    og = oracle.groups(q2k, offs, T)
+    og = oracle.groups(q2k, offs, T,
+                       dense_blocks=oracle.DENSE_BLOCKS if dense == 0 else max(dense, 0))
     assert np.array_equal(grouped, og["grouped"])
     assert counts["items"] == len(og["items"])
-    assert canonical_items(items, 4) == canonical_items(og["items"], 6)
-    cost = (items[:, 2] >> 12 & 0x1F) * np.where(items[:, 1] >= 0, 2, 1)
+    assert canonical_items(items, True) == canonical_items(og["items"], False)
+    cost = (items[:, 2] >> 12 & 0x3F) * np.where(items[:, 1] >= 0, 2, 1)
     assert (np.diff(cost) <= 0).all()
     oft = oracle.forward_tasks(pl, og["grouped"])
     assert counts["ftasks"] == len(oft)
@@ -79,6 +80,14 @@ def _check(lens, q2k, Z):
 def test_plan_bit_exact(name, Z):
     lens, q2k = STRUCTURES[name]()
     _check(lens, np.ascontiguousarray(q2k, dtype=np.int32), Z)
+
+
+@pytest.mark.parametrize("name", ["cfg3", "irregular", "long-doc"])
+@pytest.mark.parametrize("dense", [-1, 3, 32])
+def test_plan_dense_bounds(name, dense):
+    # dense octets off, a small bound, and the largest one
+    lens, q2k = STRUCTURES[name]()
+    _check(lens, np.ascontiguousarray(q2k, dtype=np.int32), 64, dense)
 
 
 def test_plan_config5():
