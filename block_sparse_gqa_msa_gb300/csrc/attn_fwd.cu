@@ -124,31 +124,54 @@ __global__ void __launch_bounds__(kKmaxThreads) k_fwd_kmax(msa_plan p, const __n
   const uint4* ksrc = reinterpret_cast<const uint4*>(K) + base;
   const uint4* vsrc = reinterpret_cast<const uint4*>(V) + base;
   uint4* vdst = v16 + base;
+  // all sixteen passes' loads in flight before any use
   float nrm = 0.f, vm = 0.f;
-#pragma unroll 4
-  for (int ps = 0; ps < kPasses; ++ps) {
-    const int row = ps * kRowsPerPass + r0;   // key row / 4, head row % 4
-    const bool ok = (row >> 2) < nkeys;
-    const int64_t i = int64_t(row) * 16 + c;
-    const uint4 x = ok ? ksrc[i] : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 y = ok ? vsrc[i] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    const uint32_t u[4] = {y.x, y.y, y.z, y.w};
-    float ss = 0.f;
+  {
+    uint4 x[kPasses];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
-      ss = fmaf(a, a, fmaf(b, b, ss));
-      vm = fmaxf(vm, fmaxf(fabsf(bf16_lo(u[e])), fabsf(bf16_hi(u[e]))));
+    for (int ps = 0; ps < kPasses; ++ps) {
+      const int row = ps * kRowsPerPass + r0;  // key row / 4, head row % 4
+      x[ps] = (row >> 2) < nkeys ? ksrc[int64_t(row) * 16 + c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float ss[kPasses];
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+      const uint32_t w[4] = {x[ps].x, x[ps].y, x[ps].z, x[ps].w};
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+        a = fmaf(lo, lo, fmaf(hi, hi, a));
+      }
+      ss[ps] = a;
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    nrm = fmaxf(nrm, sqrtf(ss));
-    if (ok)
-      vdst[i] = make_uint4(pack_f16x2(bf16_lo(u[0]), bf16_hi(u[0])),
-                           pack_f16x2(bf16_lo(u[1]), bf16_hi(u[1])),
-                           pack_f16x2(bf16_lo(u[2]), bf16_hi(u[2])),
-                           pack_f16x2(bf16_lo(u[3]), bf16_hi(u[3])));
+    for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+      for (int ps = 0; ps < kPasses; ++ps) ss[ps] += __shfl_xor_sync(0xffffffffu, ss[ps], o);
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) nrm = fmaxf(nrm, sqrtf(ss[ps]));
+  }
+  {
+    uint4 y[kPasses];
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+      const int row = ps * kRowsPerPass + r0;
+      y[ps] = (row >> 2) < nkeys ? vsrc[int64_t(row) * 16 + c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+      const int row = ps * kRowsPerPass + r0;
+      const uint32_t u[4] = {y[ps].x, y[ps].y, y[ps].z, y[ps].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        vm = fmaxf(vm, fmaxf(fabsf(bf16_lo(u[e])), fabsf(bf16_hi(u[e]))));
+      if ((row >> 2) < nkeys)
+        vdst[int64_t(row) * 16 + c] = make_uint4(pack_f16x2(bf16_lo(u[0]), bf16_hi(u[0])),
+                                                 pack_f16x2(bf16_lo(u[1]), bf16_hi(u[1])),
+                                                 pack_f16x2(bf16_lo(u[2]), bf16_hi(u[2])),
+                                                 pack_f16x2(bf16_lo(u[3]), bf16_hi(u[3])));
+    }
   }
   // per row slot r0 (head r0 % 4): the max over the 16 lanes, then over the
   // eight slots of each head
