@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(256) k_bwd_delta(msa_plan p, const __nv_bfloat
                                                    const __nv_bfloat16* dO, float* delta,
                                                    uint4* dq_pool, int64_t dq_pool_vec,
                                                    float4* dkv_pool, int64_t dkv_vec) {
+  grid_dep_wait();
+  grid_dep_release();
   // the range warning describes one backward: start this one without it
   if (blockIdx.x == 0 && threadIdx.x == 0) clear_warnings(p.header);
   if (plan_failed(p.header)) return;
@@ -359,6 +361,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     k_bwd_main(const __grid_constant__ BwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV) {
+  grid_dep_wait();
+  grid_dep_release();
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdBars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -752,6 +756,8 @@ __global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq
                                                       const float* dk_pool, const float* dv_pool,
                                                       __nv_bfloat16* dq, __nv_bfloat16* dk,
                                                       __nv_bfloat16* dv) {
+  grid_dep_wait();
+  grid_dep_release();
   if (plan_failed(p.header)) return;
   const int64_t nq = p.T * (kQHeads / 8) * (kHeadDim / 8);
   const int64_t nk8 = p.T * kKVHeads * kHeadDim / 8;
@@ -845,17 +851,22 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   // dk and dv pools are contiguous in the workspace (dv follows dk)
   const int64_t dkv_vec = int64_t(L.off_dv - L.off_dk) / 16 + p.T * kKVHeads * kHeadDim / 4;
   const int64_t warps = (rows + kDeltaRowsPerWarp - 1) / kDeltaRowsPerWarp;
+  // The first kernel waits for the caller's work in the stream; each later
+  // one may overlap its predecessor's tail (launch_k).
   launch_begin("bwd_delta", s);
-  k_bwd_delta<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
-      static_cast<uint4*>(dq_pool), dq_vec, reinterpret_cast<float4*>(dk_pool), dkv_vec);
+  cudaError_t e = launch_k(false, k_bwd_delta, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, p,
+                           static_cast<const __nv_bfloat16*>(o),
+                           static_cast<const __nv_bfloat16*>(dout), delta,
+                           static_cast<uint4*>(dq_pool), dq_vec,
+                           reinterpret_cast<float4*>(dk_pool), dkv_vec);
   launch_end("bwd_delta", s);
+  if (e != cudaSuccess) return e;
 
   static bool attr_set = false;
   if (!attr_set) {
     for (auto fn : {k_bwd_main<MSA_DQ_ACCUM_F16>, k_bwd_main<MSA_DQ_ACCUM_BF16>,
                     k_bwd_main<MSA_DQ_ACCUM_F32>}) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
       if (e != cudaSuccess) return e;
     }
     attr_set = true;
@@ -863,19 +874,18 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   BwdParams prm{p, lse, delta, dq_pool, dk_pool, dv_pool, scale * kLog2e, scale, p.dq_accum};
   launch_begin("bwd_main", s);
   const unsigned grid = unsigned(device_sm_count());
-  if (p.dq_accum == MSA_DQ_ACCUM_F32)
-    k_bwd_main<MSA_DQ_ACCUM_F32><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
-  else if (p.dq_accum == MSA_DQ_ACCUM_BF16)
-    k_bwd_main<MSA_DQ_ACCUM_BF16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
-  else
-    k_bwd_main<MSA_DQ_ACCUM_F16><<<grid, kBwdThreads, kBwdSmem, s>>>(prm, mQ, mDO, mK, mV);
+  auto main_fn = p.dq_accum == MSA_DQ_ACCUM_F32    ? k_bwd_main<MSA_DQ_ACCUM_F32>
+                 : p.dq_accum == MSA_DQ_ACCUM_BF16 ? k_bwd_main<MSA_DQ_ACCUM_BF16>
+                                                   : k_bwd_main<MSA_DQ_ACCUM_F16>;
+  e = launch_k(true, main_fn, dim3(grid), dim3(kBwdThreads), kBwdSmem, s, prm, mQ, mDO, mK, mV);
   launch_end("bwd_main", s);
+  if (e != cudaSuccess) return e;
   launch_begin("bwd_finalize", s);
-  k_bwd_finalize<<<unsigned(device_sm_count() * 8), 256, 0, s>>>(
-      p, dq_pool, dk_pool, dv_pool, static_cast<__nv_bfloat16*>(dq),
-      static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
+  e = launch_k(true, k_bwd_finalize, dim3(grid * 8), dim3(256), 0, s, p, (const void*)dq_pool,
+               (const float*)dk_pool, (const float*)dv_pool, static_cast<__nv_bfloat16*>(dq),
+               static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
   launch_end("bwd_finalize", s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kKmaxThreads) k_fwd_kmax(msa_plan p, const __n
                                                            const __nv_bfloat16* V, float* kmax,
                                                            float* vmax, int32_t* list,
                                                            uint4* v16) {
+  grid_dep_wait();
+  grid_dep_release();
   constexpr int kRowsPerPass = kKmaxThreads / 16;              // 32 rows per pass
   constexpr int kPasses = kBlock * kKVHeads / kRowsPerPass;    // 16 passes
   __shared__ float hk[kRowsPerPass], hv[kRowsPerPass];
@@ -210,6 +212,8 @@ __device__ __forceinline__ float v_scale_in(float vmax) {
 }
 __global__ void __launch_bounds__(256) k_fwd_v16(msa_plan p, const __nv_bfloat16* V,
                                                  const float* vmax, uint4* v16, float* vscale) {
+  grid_dep_wait();
+  grid_dep_release();
   __shared__ float red[8][4];
   if (plan_failed(p.header)) return;
   const int64_t NB = p.header[kHdrNB];
@@ -274,6 +278,8 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
                                                   const float* kmax, const float* vmax,
                                                   float c2, float* M2, float* lsum,
                                                   float* pool) {
+  grid_dep_wait();
+  grid_dep_release();
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
@@ -590,6 +596,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_main(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                const __grid_constant__ CUtensorMap mapPool) {
+  grid_dep_wait();
+  grid_dep_release();
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdBars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -1082,6 +1090,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     k_fwd_group(const __grid_constant__ FwdParams prm, const __grid_constant__ CUtensorMap mapQ,
                 const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV) {
+  grid_dep_wait();
+  grid_dep_release();
   extern __shared__ uint8_t smem_raw[];
   __shared__ GrpBars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -1331,6 +1341,8 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
                                                       const float* lsum, const float* pool,
                                                       __nv_bfloat16* O, float* lse,
                                                       int32_t* list) {
+  grid_dep_wait();
+  grid_dep_release();
   if (plan_failed(p.header)) return;
   const int lane = threadIdx.x & 31, sub = lane & 15;
   const int64_t rows = p.T * kQHeads;
@@ -1383,6 +1395,8 @@ __global__ void __launch_bounds__(256) k_fwd_fallback(msa_plan p, const __nv_bfl
                                                       const __nv_bfloat16* V, float c2,
                                                       const int32_t* list, __nv_bfloat16* O,
                                                       float* lse) {
+  grid_dep_wait();
+  grid_dep_release();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = int64_t(gridDim.x) * blockDim.x / 32;
   const int32_t n = list[0];
@@ -1466,17 +1480,11 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
       make_map_pool32(&mPool, pool, p.T * kQHeads) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k);
+  const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(v);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   cudaError_t e;
-  launch_begin("fwd_kmax", s);
-  k_fwd_kmax<<<unsigned(p.nb_cap), kKmaxThreads, 0, s>>>(p, static_cast<const __nv_bfloat16*>(k),
-                                                static_cast<const __nv_bfloat16*>(v), kmax, vmax,
-                                                list, v16);
-  launch_end("fwd_kmax", s);
-  launch_begin("fwd_v16", s);
-  k_fwd_v16<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(v), vmax, v16, vscale);
-  launch_end("fwd_v16", s);
-
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(k_fwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
@@ -1485,33 +1493,47 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  FwdParams prm{p,    M2,   kmax, vmax, pool, lsum, list, static_cast<__nv_bfloat16*>(o),
-                lse,  vscale, c2};
+  FwdParams prm{p, M2, kmax, vmax, pool, lsum, list, ob, lse, vscale, c2};
   const unsigned grid = unsigned(device_sm_count());
+  // The first kernel waits for the caller's work in the stream; each later
+  // one may overlap its predecessor's tail (launch_k).
+  launch_begin("fwd_kmax", s);
+  e = launch_k(false, k_fwd_kmax, dim3(unsigned(p.nb_cap)), dim3(kKmaxThreads), 0, s, p, kb, vb,
+               kmax, vmax, list, v16);
+  launch_end("fwd_kmax", s);
+  if (e != cudaSuccess) return e;
+  launch_begin("fwd_v16", s);
+  e = launch_k(true, k_fwd_v16, dim3(grid * 4), dim3(256), 0, s, p, vb, (const float*)vmax, v16,
+               vscale);
+  launch_end("fwd_v16", s);
+  if (e != cudaSuccess) return e;
   // The group kernel needs neither the row shifts nor the pool: it runs
   // first, on the K / V / Q lines the earlier kernels left in L2.
   launch_begin("fwd_group", s);
-  k_fwd_group<<<grid, kGrpThreads, kGrpSmem, s>>>(prm, mQ, mK, mV);
+  e = launch_k(true, k_fwd_group, dim3(grid), dim3(kGrpThreads), kGrpSmem, s, prm, mQ, mK, mV);
   launch_end("fwd_group", s);
+  if (e != cudaSuccess) return e;
   const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
-  k_fwd_rows<<<unsigned((warps + 7) / 8), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), kmax, vmax, c2, M2, lsum, pool);
+  e = launch_k(true, k_fwd_rows, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, p, qb,
+               (const float*)kmax, (const float*)vmax, c2, M2, lsum, pool);
   launch_end("fwd_rows", s);
-
+  if (e != cudaSuccess) return e;
   launch_begin("fwd_main", s);
-  k_fwd_main<<<grid, kFwdThreads, kFwdSmem, s>>>(prm, mQ, mK, mV, mPool);
+  e = launch_k(true, k_fwd_main, dim3(grid), dim3(kFwdThreads), kFwdSmem, s, prm, mQ, mK, mV,
+               mPool);
   launch_end("fwd_main", s);
+  if (e != cudaSuccess) return e;
   launch_begin("fwd_finalize", s);
-  k_fwd_finalize<<<grid * 16, 256, 0, s>>>(p, M2, lsum, pool, static_cast<__nv_bfloat16*>(o),
-                                           lse, list);
+  e = launch_k(true, k_fwd_finalize, dim3(grid * 16), dim3(256), 0, s, p, (const float*)M2,
+               (const float*)lsum, (const float*)pool, ob, lse, list);
   launch_end("fwd_finalize", s);
+  if (e != cudaSuccess) return e;
   launch_begin("fwd_fallback", s);
-  k_fwd_fallback<<<unsigned(device_sm_count() * 4), 256, 0, s>>>(
-      p, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), c2, list, static_cast<__nv_bfloat16*>(o), lse);
+  e = launch_k(true, k_fwd_fallback, dim3(grid * 4), dim3(256), 0, s, p, qb, kb, vb, c2,
+               (const int32_t*)list, ob, lse);
   launch_end("fwd_fallback", s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

@@ -169,6 +169,39 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
   return L;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_k(true, ...)
+// may start while the previous kernel on the stream is still finishing (its
+// launch and prologue overlap that kernel's tail); every kernel therefore
+// calls grid_dep_wait() before it touches global memory, which returns once
+// the previous kernel has completed and its writes are visible (at once for
+// a kernel launched without the attribute), and then grid_dep_release(),
+// which lets the next kernel launch.  Since every kernel waits for its
+// predecessor, a kernel's completion implies that of all before it.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Profiling on (msa_profile_enable): launches are then kept apart by the
+// timing events and take no programmatic overlap.
+bool profiling_on();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (overlap && !profiling_on()) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Kernel-launch bookkeeping (profiling hooks, launch counter) - msa_api.cu.
 // launch_end counts `kernels` launches under `name`.
 void launch_begin(const char* name, cudaStream_t s);

@@ -67,6 +67,8 @@ void drain(Prof& p, bool wait) {
 }
 }  // namespace
 
+bool profiling_on() { return prof().on; }
+
 void launch_begin(const char* name, cudaStream_t s) {
   (void)name;
   Prof& p = prof();

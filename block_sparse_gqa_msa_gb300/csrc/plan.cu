@@ -71,6 +71,8 @@ __device__ Tv block_excl_scan(Tv x, Tv* total) {
 
 // ------------------------------------------------------------ documents
 __global__ void __launch_bounds__(1024) k_plan_docs(msa_plan p) {
+  grid_dep_wait();
+  grid_dep_release();
   __shared__ int bad;
   __shared__ int64_t tot_nb, tot_tri;
   const int32_t* offs = p.doc_offsets;
@@ -127,7 +129,9 @@ __global__ void __launch_bounds__(1024) k_plan_docs(msa_plan p) {
 enum BlockPass { kPassCount = 0, kPassScatter = 1, kPassEmit = 2 };
 
 template <int PASS>
-__global__ void __launch_bounds__(128) k_plan_blocks(msa_plan p) {
+__global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
+  grid_dep_wait();
+  grid_dep_release();
   __shared__ uint32_t bm[kChunkV][4];
   __shared__ int s_doc, s_skip;
   __shared__ unsigned long long s_pairs;
@@ -414,6 +418,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const int32_t* in, int32_
                                                        int64_t* total, unsigned long long* st,
                                                        int64_t* hdr, const int4* csrc,
                                                        int4* cdst) {
+  grid_dep_wait();
+  grid_dep_release();
   __shared__ int64_t tot, excl_sh;
   __shared__ unsigned tile_sh;
   // A failed plan's counts are not to be trusted (an earlier pass stopped
@@ -501,32 +507,38 @@ cudaError_t scan(const msa_plan& p, int k, const int32_t* in, int32_t* out, cons
   const unsigned grid = unsigned((cap + kScanTile - 1) / kScanTile);
   if (grid == 0) return cudaSuccess;
   launch_begin(k == 2 ? "plan_ftasks" : "plan_scan", s);
-  k_scan<<<grid, kScanThreads, 0, s>>>(in, out, n_ptr, cap, total, scan_status(p, k), p.header,
-                                       csrc, cdst);
+  const cudaError_t e = launch_k(true, k_scan, dim3(grid), dim3(kScanThreads), 0, s, in, out, n_ptr,
+                                 cap, total, scan_status(p, k), p.header, csrc, cdst);
   launch_end(k == 2 ? "plan_ftasks" : "plan_scan", s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const msa_plan& p, cudaStream_t s) {
+  // the first kernel waits for the caller's work in the stream; each later
+  // one may overlap its predecessor's tail (launch_k)
   launch_begin("plan_docs", s);
-  k_plan_docs<<<1, 1024, 0, s>>>(p);
+  cudaError_t e = launch_k(false, k_plan_docs, dim3(1), dim3(1024), 0, s, p);
   launch_end("plan_docs", s);
+  if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(4 * p.nb_cap);
   launch_begin("plan_count", s);
-  k_plan_blocks<kPassCount><<<grid, 128, 0, s>>>(p);
+  e = launch_k(true, k_plan_blocks<kPassCount>, dim3(grid), dim3(128), 0, s, p);
   launch_end("plan_count", s);
-  cudaError_t e = scan(p, 0, p.cnt, p.off, p.header + kHdrTri, p.tri_cap, p.header + kHdrNnz, s);
+  if (e != cudaSuccess) return e;
+  e = scan(p, 0, p.cnt, p.off, p.header + kHdrTri, p.tri_cap, p.header + kHdrNnz, s);
   if (e != cudaSuccess) return e;
   launch_begin("plan_scatter", s);
-  k_plan_blocks<kPassScatter><<<grid, 128, 0, s>>>(p);
+  e = launch_k(true, k_plan_blocks<kPassScatter>, dim3(grid), dim3(128), 0, s, p);
   launch_end("plan_scatter", s);
+  if (e != cudaSuccess) return e;
   e = scan(p, 1, p.tcnt, p.toff, p.header + kHdrTri, p.tri_cap, p.header + kHdrTasks, s);
   if (e != cudaSuccess) return e;
   launch_begin("plan_emit", s);
-  k_plan_blocks<kPassEmit><<<grid, 128, 0, s>>>(p);
+  e = launch_k(true, k_plan_blocks<kPassEmit>, dim3(grid), dim3(128), 0, s, p);
   launch_end("plan_emit", s);
+  if (e != cudaSuccess) return e;
   // the forward's pooled list: tasks with fflag set, in task order
   return scan(p, 2, p.fflag, p.fpos, p.header + kHdrTasks, p.task_cap, p.header + kHdrFTasks, s,
               reinterpret_cast<const int4*>(p.tasks), reinterpret_cast<int4*>(p.ftasks));
