@@ -1246,15 +1246,28 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           break;
         }
         tc_fence_after();
-        const bool full = __all_sync(0xffffffffu, jmax == kBlock - 1);
+        // Without masks when every row of the warp sees the whole block or
+        // none of it (a dense item's token that did not select the block):
+        // such rows are computed unmasked and then zeroed.
+        const bool full = __all_sync(0xffffffffu, jmax == kBlock - 1 || jmax < 0);
         if (j == 0) {  // the item's first block sets the reference
           const float mx = full ? tile_row_max<false>(cs, jmax) : tile_row_max<true>(cs, jmax);
           mref = jmax >= 0 ? mx * prm.c2 : -INFINITY;
         }
         uint32_t pk[64];
         float tmax;
-        float ls = full ? row_exp_regs<false>(cs, jmax, prm.c2, mref, pk, &tmax)
-                        : row_exp_regs<true>(cs, jmax, prm.c2, mref, pk, &tmax);
+        auto row_exp = [&]() {
+          if (!full) return row_exp_regs<true>(cs, jmax, prm.c2, mref, pk, &tmax);
+          float l = row_exp_regs<false>(cs, jmax, prm.c2, mref, pk, &tmax);
+          if (jmax < 0) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) pk[k] = 0u;
+            l = 0.f;
+            tmax = -INFINITY;
+          }
+          return l;
+        };
+        float ls = row_exp();
         const float mxc = tmax * prm.c2;
         const bool raise = j > 0 && jmax >= 0 && mxc > mref + kRaiseOctaves;
         if (__any_sync(0xffffffffu, raise)) {
@@ -1273,8 +1286,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
             tmem_st32_nc(co + 32 * c, o);
           }
-          ls = full ? row_exp_regs<false>(cs, jmax, prm.c2, mref, pk, &tmax)
-                    : row_exp_regs<true>(cs, jmax, prm.c2, mref, pk, &tmax);
+          ls = row_exp();
         }
         lsum += ls;
         // P over the first 64 columns of S (all of S has been read)
