@@ -160,27 +160,15 @@ struct BwdParams {
   int dq_accum;
 };
 
-// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
-// index arithmetic runs on the MMA issuer's critical path).
+// Tasks per chunk of the CTA walk (TaskWalk: full rounds of chunks go
+// round-robin over the CTAs, the rest is split evenly).
 constexpr int kBwdChunk = 64;
-__device__ __forceinline__ int64_t cta_task(int64_t i) {
-  return (int64_t(blockIdx.x) + (i / kBwdChunk) * gridDim.x) * kBwdChunk + (i % kBwdChunk);
-}
-__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
-  constexpr int chunk = kBwdChunk;
-  const int64_t nchunks = (ntasks + chunk - 1) / chunk;
-  if (int64_t(blockIdx.x) >= nchunks) return 0;
-  const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;
-  const int64_t last_chunk = blockIdx.x + (mine - 1) * gridDim.x;
-  return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
-                                                                    : chunk);
-}
 // Task record i of this CTA's walk; past the end, the last one (every
 // caller guards its uses by the index).  Only the address depends on the
 // index test, never the loaded value, so nothing waits for the load until
 // the record is used.  With no tasks, entry 0 of the (allocated) table.
-__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
-  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, const TaskWalk& w) {
+  return tasks[w.n > 0 ? walk_task<kBwdChunk>(w, i < w.n ? i : w.n - 1) : 0];
 }
 __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
@@ -199,8 +187,9 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
 // soon as P^T(t) is in TMEM, and the compute warps read dQ^T(t) out while
 // S^T(t+1) runs.
 __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t sbase,
-                                          const int4* tasks, int64_t my_n,
+                                          const int4* tasks, const TaskWalk walk,
                                           volatile int* abort_flag) {
+  const int64_t my_n = walk.n;
   constexpr uint32_t idKK = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
   constexpr uint32_t idKM = idesc_bf16_f32(128, 128, 0, 1);  // dV, dK (A in TMEM)
   constexpr uint32_t idMM = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T
@@ -257,8 +246,8 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   };
   int64_t kv_loads = 1, seg_done = 0;
   bool first_in_seg = true;
-  int cur_kv = task_rec(tasks, 0, my_n).w;
-  int next_kv = task_rec(tasks, 1, my_n).w;
+  int cur_kv = task_rec(tasks, 0, walk).w;
+  int next_kv = task_rec(tasks, 1, walk).w;
   bool ok = wait(bars.kv_full, 0) && wait(bars.qdo_full[0], 0);
   if (ok) {
     issue_S(0);
@@ -266,7 +255,7 @@ __device__ __noinline__ void bwd_mma_role(BwdBars& bars, uint32_t tmem, uint32_t
   }
   for (int64_t it = 0; ok && it < my_n; ++it) {
     const uint32_t ph = uint32_t(it & 1);
-    const int next2_kv = task_rec(tasks, it + 2, my_n).w;  // used next iteration
+    const int next2_kv = task_rec(tasks, it + 2, walk).w;  // used next iteration
     const uint32_t acc0 = first_in_seg ? 0u : 1u;
     // the first dV / dK of a run overwrite the accumulators: the reducers
     // must have flushed the previous run
@@ -412,7 +401,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrTasks];
-  const int64_t my_n = cta_task_count(ntasks);
+  const TaskWalk walk = task_walk<kBwdChunk>(ntasks);
+  const int64_t my_n = walk.n;
   const int4* tasks = reinterpret_cast<const int4*>(p.tasks);
 
   if (warp == 0) {
@@ -424,7 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
-      int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
+      int4 rec = task_rec(tasks, 0, walk), rec1 = task_rec(tasks, 1, walk);
       int32_t tok[kTaskQueries];
       {
         const TaskView tv = decode_task(rec);
@@ -433,7 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       for (; it < my_n; ++it) {
         const TaskView tv = decode_task(rec);
-        const int4 rec2 = task_rec(tasks, it + 2, my_n);
+        const int4 rec2 = task_rec(tasks, it + 2, walk);
         int32_t tok1[kTaskQueries];
         {
           const TaskView tv1 = decode_task(rec1);
@@ -488,7 +478,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, my_n, abort_flag);
+    if (lane == 0 && my_n > 0) bwd_mma_role(bars, tmem, sbase, tasks, walk, abort_flag);
   } else if (warp < 10) {
     // ---------------- compute (thread = TMEM lane; half = block of 64 q-rows)
     // Phase 1 (after S^T; thread = key): P = 2^(S^T c2 - LSE log2 e), masked
@@ -524,7 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool wf = __all_sync(0xffffffffu, jl == kBlock - 1);
       if (lane == 0) s_wfull[quad] = wf ? 1 : 0;
     };
-    int4 rec0 = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
+    int4 rec0 = task_rec(tasks, 0, walk), rec1 = task_rec(tasks, 1, walk);
     int32_t tok1 = 0;
     if (my_n > 0) {
       tok1 = task_token(p.col, decode_task(rec1), qi);
@@ -567,7 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int64_t it = 0; cols_ok && it < my_n; ++it) {
       const uint32_t ph = uint32_t(it & 1);
       const int st = int(it & 1);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n);
+      const int4 rec2 = task_rec(tasks, it + 2, walk);
       // The next task's column scalars: loaded now (unconditionally, so no
       // select waits for them here), stored by half 0 after phase 2.
       const TaskView tv1 = decode_task(rec1);
@@ -680,11 +670,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quad = warp & 3;
     const int key = quad * 32 + lane;
     const uint32_t lane_base = uint32_t(quad * 32) << 16;
-    int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
+    int4 rec = task_rec(tasks, 0, walk), rec1 = task_rec(tasks, 1, walk);
     int64_t nseg = 0;
     for (int64_t it = 0; it < my_n; ++it) {
       const TaskView tv = decode_task(rec);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n);
+      const int4 rec2 = task_rec(tasks, it + 2, walk);
       int32_t ta[2], tb[2];  // tokens of queries 2, 3 and 6, 7
 #pragma unroll
       for (int k = 0; k < 2; ++k) {

@@ -495,29 +495,15 @@ struct FwdParams {
   float c2;
 };
 
-// Task i of the CTA's walk: chunks of kFwdChunk consecutive tasks go round-robin
-// over the CTAs, so all CTAs advance through the task list together.
-// Tasks per chunk of the CTA walk (a compile-time power of two: the walk's
-// index arithmetic runs on the MMA issuer's critical path).
+// Tasks per chunk of the CTA walk (TaskWalk: full rounds of chunks go
+// round-robin over the CTAs, the rest is split evenly).
 constexpr int kFwdChunk = 16;
-__device__ __forceinline__ int64_t cta_task(int64_t i) {
-  return (int64_t(blockIdx.x) + (i / kFwdChunk) * gridDim.x) * kFwdChunk + (i % kFwdChunk);
-}
-__device__ __forceinline__ int64_t cta_task_count(int64_t ntasks) {
-  constexpr int chunk = kFwdChunk;
-  const int64_t nchunks = (ntasks + chunk - 1) / chunk;
-  if (int64_t(blockIdx.x) >= nchunks) return 0;
-  const int64_t mine = (nchunks - 1 - blockIdx.x) / gridDim.x + 1;  // chunks of this CTA
-  const int64_t last_chunk = blockIdx.x + (mine - 1) * gridDim.x;
-  return (mine - 1) * chunk + (ntasks - last_chunk * chunk < chunk ? ntasks - last_chunk * chunk
-                                                                    : chunk);
-}
 // Task record i of this CTA's walk; past the end, the last one (every
 // caller guards its uses by the index).  Only the address depends on the
 // index test, never the loaded value, so nothing waits for the load until
 // the record is used.  With no tasks, entry 0 of the (allocated) table.
-__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, int64_t n) {
-  return tasks[n > 0 ? cta_task(i < n ? i : n - 1) : 0];
+__device__ __forceinline__ int4 task_rec(const int4* tasks, int64_t i, const TaskWalk& w) {
+  return tasks[w.n > 0 ? walk_task<kFwdChunk>(w, i < w.n ? i : w.n - 1) : 0];
 }
 __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView& tv, int qi) {
   return col[tv.col_begin + (qi < tv.nq ? qi : tv.nq - 1)];
@@ -526,8 +512,9 @@ __device__ __forceinline__ int32_t task_token(const int32_t* col, const TaskView
 // MMA issuer of k_fwd_main (one thread).  A function of its own so its few
 // live values stay in registers whatever the other roles need.
 __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t sbase,
-                                          const int4* tasks, int64_t my_n,
+                                          const int4* tasks, const TaskWalk walk,
                                           volatile int* abort_flag) {
+  const int64_t my_n = walk.n;
   constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // Q . K^T   (bf16)
   constexpr uint32_t idPV = idesc_f16_f32(128, 128, 0, 1);  // P . V     (fp16, P in TMEM)
   auto wait = [&](uint64_t& bar, uint32_t ph) {
@@ -563,12 +550,12 @@ __device__ __noinline__ void fwd_mma_role(FwdBars& bars, uint32_t tmem, uint32_t
     ++kv_loads;
     return true;
   };
-  int cur_kv = task_rec(tasks, 0, my_n).w;
-  int next_kv = task_rec(tasks, 1, my_n).w;
+  int cur_kv = task_rec(tasks, 0, walk).w;
+  int next_kv = task_rec(tasks, 1, walk).w;
   ok = wait_kv() && issue_S(0);
   for (int64_t it = 0; ok && it < my_n; ++it) {
     const int st = int(it & 1);
-    const int next2_kv = task_rec(tasks, it + 2, my_n).w;
+    const int next2_kv = task_rec(tasks, it + 2, walk).w;
     const bool same = (it + 1 < my_n) && next_kv == cur_kv;
     if (same && !issue_S(it + 1)) break;
     if (!wait(bars.p_full[st], uint32_t((it >> 1) & 1))) break;
@@ -638,7 +625,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int64_t ntasks = skip_sh ? 0 : p.header[kHdrFTasks];
-  const int64_t my_n = cta_task_count(ntasks);
+  const TaskWalk walk = task_walk<kFwdChunk>(ntasks);
+  const int64_t my_n = walk.n;
   const int4* tasks = reinterpret_cast<const int4*>(p.ftasks);
 
   if (warp == 0) {
@@ -649,7 +637,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mapV);
       int prev_kv = -1;
       int64_t kv_loads = 0, it = 0;
-      int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
+      int4 rec = task_rec(tasks, 0, walk), rec1 = task_rec(tasks, 1, walk);
       int32_t tok[kTaskQueries];
       {
         const TaskView tv = decode_task(rec);
@@ -658,7 +646,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       for (; it < my_n; ++it) {
         const TaskView tv = decode_task(rec);
-        const int4 rec2 = task_rec(tasks, it + 2, my_n);
+        const int4 rec2 = task_rec(tasks, it + 2, walk);
         int32_t tok1[kTaskQueries];
         {
           const TaskView tv1 = decode_task(rec1);
@@ -701,7 +689,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, my_n, abort_flag);
+    if (lane == 0 && my_n > 0) fwd_mma_role(bars, tmem, sbase, tasks, walk, abort_flag);
   } else if (warp < 10) {
     // ---------------- softmax (warps 2-5: even tasks, 6-9: odd tasks)
     const int quad = warp & 3;
@@ -720,11 +708,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // runs, in two steps so no load result is consumed right after it is
     // issued: the row's token at the top of task it, its shift M and
     // grouped flag after the exponentials.
-    int4 rec1 = task_rec(tasks, par + 2, my_n);
+    int4 rec1 = task_rec(tasks, par + 2, walk);
     int jmax_c = -1;
     float m2_c = 0.f;
     if (par < my_n) {
-      const TaskView tv = decode_task(task_rec(tasks, par, my_n));
+      const TaskView tv = decode_task(task_rec(tasks, par, walk));
       const int32_t tok = task_token(p.col, tv, qi);
       jmax_c = row_jmax(tv, tok);
       m2_c = prm.M2[int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh];
@@ -733,7 +721,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int st = int(it & 1);
       const int jmax = jmax_c;
       const float m2 = m2_c;
-      const int4 rec2 = task_rec(tasks, it + 4, my_n);
+      const int4 rec2 = task_rec(tasks, it + 4, walk);
       // (loads of the next task's row data are unconditional - rec1 is a
       // valid record even past the end - so nothing waits for them here)
       const int32_t ntok = task_token(p.col, decode_task(rec1), qi);
@@ -788,13 +776,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t stage_row = stage_q + uint32_t(hh) * 128u;
     const uint32_t swz = uint32_t(hh & 7);
     if (lane == 0 && my_n > 0) tma_prefetch_desc(&mapPool);
-    int4 rec = task_rec(tasks, 0, my_n), rec1 = task_rec(tasks, 1, my_n);
+    int4 rec = task_rec(tasks, 0, walk), rec1 = task_rec(tasks, 1, walk);
     // the row's token is loaded one task ahead
     int32_t tok_c = my_n > 0 ? task_token(p.col, decode_task(rec), qi) : 0;
     for (int64_t it = 0; it < my_n; ++it) {
       const int st = int(it & 1);
       const TaskView tv = decode_task(rec);
-      const int4 rec2 = task_rec(tasks, it + 2, my_n);
+      const int4 rec2 = task_rec(tasks, it + 2, walk);
       const int32_t tok = tok_c;
       tok_c = task_token(p.col, decode_task(rec1), qi);  // rec1: a valid record
       const int64_t grow = int64_t(tok) * kQHeads + tv.g * kHeadsPerGroup + hh;

@@ -202,6 +202,36 @@ cudaError_t launch_k(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 blo
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// A CTA's share of a persistent kernel's task list of n tasks, walked in
+// chunks of C consecutive tasks (C a power of two, so the walk's index
+// arithmetic stays cheap on the MMA issuer's path): full rounds of G chunks
+// go round-robin over the G CTAs, so all CTAs advance through the list
+// together; the tasks after the last full round are split evenly, so that
+// the CTAs' counts differ by at most one task.
+struct TaskWalk {
+  int64_t n;      // tasks of this CTA
+  int64_t full;   // of them, in full rounds
+  int64_t tail0;  // first task of this CTA's share of the rest
+};
+template <int C>
+__device__ __forceinline__ TaskWalk task_walk(int64_t ntasks) {
+  const int64_t G = gridDim.x, c = blockIdx.x;
+  const int64_t R = ntasks / (G * C);
+  const int64_t rest = ntasks - R * G * C;
+  const int64_t q = rest / G, extra = rest % G;
+  TaskWalk w;
+  w.full = R * C;
+  w.tail0 = R * G * C + c * q + (c < extra ? c : extra);
+  w.n = w.full + q + (c < extra ? 1 : 0);
+  return w;
+}
+// Task index (into the list) of the CTA's i-th task.
+template <int C>
+__device__ __forceinline__ int64_t walk_task(const TaskWalk& w, int64_t i) {
+  return i < w.full ? (int64_t(blockIdx.x) + (i / C) * gridDim.x) * C + (i % C)
+                    : w.tail0 + (i - w.full);
+}
+
 // Kernel-launch bookkeeping (profiling hooks, launch counter) - msa_api.cu.
 // launch_end counts `kernels` launches under `name`.
 void launch_begin(const char* name, cudaStream_t s);
