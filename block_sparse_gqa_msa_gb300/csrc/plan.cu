@@ -272,13 +272,16 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
         }
       }
     } else {  // kPassEmit
-      // Heads in this CTA: v == qb, and every v < lo_q when qb == lo_q.
-      const int64_t vbeg = (qb == lo_q) ? c0 : (qb >= c0 ? qb : cend + 1);
-      for (int64_t v = vbeg; v <= cend; ++v) {
-        if (qb != lo_q && v != qb) continue;
-        if (qb == lo_q && v > qb) continue;
+      // Head entries (v, first = max(v, lo_q)) own their run's tasks.  The
+      // head of v >= lo_q is emitted by the CTA of query block v; the heads
+      // of the key blocks before the super-block (v < lo_q, all in query
+      // block lo_q) are spread over the super-block's CTAs, v modulo its
+      // length, so that no CTA walks all of them.
+      const int64_t span = hi_q - lo_q;
+      for (int64_t v = c0; v <= cend; ++v) {
+        if (v >= lo_q ? v != qb : v % span != qb - lo_q) continue;
         const int64_t first = v > lo_q ? v : lo_q;
-        const int64_t e = seg + tri_local(n, Zs, v, qb);
+        const int64_t e = seg + tri_local(n, Zs, v, first);
         const int64_t last = e + (hi_q - first) - 1;
         const int64_t len = int64_t(p.off[last]) + p.cnt[last] - p.off[e];
         const int nt = p.tcnt[e];
