@@ -412,25 +412,30 @@ def run_gpu(args, rank, world):
         e[0].record(stream)
         p = api.msa_build_plan(q2k, offs, super_block=args.super_block,
                                  workspace=pws)
-        e[1].record(stream)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
-        e[2].record(stream)
         api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
         e[3].record(stream)
     torch.cuda.synchronize()
     launches = api.launch_count() - launches0
     clk = clocks.stop() if clocks else None
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     # ---- per-kernel times: a separate loop of the same steps with the
     # library's per-launch events (they keep launches apart, so the timed
     # loop above runs without them)
     psteps = min(args.steps, 5)
     api.profile_enable(True)
     api.profile_reset()
+    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(psteps)]
     for i in range(psteps):
         flush.zero_()
+        e = pevs[i]
+        e[0].record(stream)
         p = api.msa_build_plan(q2k, offs, super_block=args.super_block, workspace=pws)
+        e[1].record(stream)
         api.msa_forward(p, q, k, v, w.scale, o=o, lse=lse, workspace=fws)
+        e[2].record(stream)
         api.msa_backward(p, q, k, v, o, lse, do, w.scale, dq=dq, dk=dk, dv=dv, workspace=bws)
+        e[3].record(stream)
     torch.cuda.synchronize()
     kern = {}
     for name in KERNELS:
@@ -440,10 +445,10 @@ def run_gpu(args, rank, world):
     api.profile_enable(False)
     if world > 1:
         torch.distributed.barrier()
-    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [a + b + c for a, b, c in zip(plan_ms, fwd_ms, bwd_ms)]
+    # the plan / forward / backward split, from the profiled loop
+    plan_ms = [e[0].elapsed_time(e[1]) for e in pevs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in pevs]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in pevs]
     flop_step = flop_fwd + flop_bwd
     ms_per_step, value, tok_s = aggregate(sum(step_ms), args.steps, flop_step, T, world)
 

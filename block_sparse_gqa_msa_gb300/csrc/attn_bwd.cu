@@ -841,10 +841,11 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   // dk and dv pools are contiguous in the workspace (dv follows dk)
   const int64_t dkv_vec = int64_t(L.off_dv - L.off_dk) / 16 + p.T * kKVHeads * kHeadDim / 4;
   const int64_t warps = (rows + kDeltaRowsPerWarp - 1) / kDeltaRowsPerWarp;
-  // The first kernel waits for the caller's work in the stream; each later
-  // one may overlap its predecessor's tail (launch_k).
+  // Every kernel may start during its predecessor's tail (launch_k) and
+  // waits for it before touching memory; a caller's kernel that never
+  // signals counts as signalling when it completes.
   launch_begin("bwd_delta", s);
-  cudaError_t e = launch_k(false, k_bwd_delta, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, p,
+  cudaError_t e = launch_k(true, k_bwd_delta, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, p,
                            static_cast<const __nv_bfloat16*>(o),
                            static_cast<const __nv_bfloat16*>(dout), delta,
                            static_cast<uint4*>(dq_pool), dq_vec,

@@ -1495,10 +1495,11 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   }
   FwdParams prm{p, M2, kmax, vmax, pool, lsum, list, ob, lse, vscale, c2};
   const unsigned grid = unsigned(device_sm_count());
-  // The first kernel waits for the caller's work in the stream; each later
-  // one may overlap its predecessor's tail (launch_k).
+  // Every kernel may start during its predecessor's tail (launch_k) and
+  // waits for it before touching memory; a caller's kernel that never
+  // signals counts as signalling when it completes.
   launch_begin("fwd_kmax", s);
-  e = launch_k(false, k_fwd_kmax, dim3(unsigned(p.nb_cap)), dim3(kKmaxThreads), 0, s, p, kb, vb,
+  e = launch_k(true, k_fwd_kmax, dim3(unsigned(p.nb_cap)), dim3(kKmaxThreads), 0, s, p, kb, vb,
                kmax, vmax, list, v16);
   launch_end("fwd_kmax", s);
   if (e != cudaSuccess) return e;

@@ -174,9 +174,11 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
 // launch and prologue overlap that kernel's tail); every kernel therefore
 // calls grid_dep_wait() before it touches global memory, which returns once
 // the previous kernel has completed and its writes are visible (at once for
-// a kernel launched without the attribute), and then grid_dep_release(),
-// which lets the next kernel launch.  Since every kernel waits for its
-// predecessor, a kernel's completion implies that of all before it.
+// a kernel launched without the attribute; a previous kernel that never
+// calls grid_dep_release() releases its dependents when it completes), and
+// then grid_dep_release(), which lets the next kernel launch.  Since every
+// kernel waits for its predecessor, a kernel's completion implies that of
+// all before it.  Copies and event waits in the stream keep their order.
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -519,10 +519,11 @@ cudaError_t scan(const msa_plan& p, int k, const int32_t* in, int32_t* out, cons
 }  // namespace
 
 cudaError_t launch_plan(const msa_plan& p, cudaStream_t s) {
-  // the first kernel waits for the caller's work in the stream; each later
-  // one may overlap its predecessor's tail (launch_k)
+  // Every kernel may start during its predecessor's tail (launch_k) and
+  // waits for it before touching memory; a caller's kernel that never
+  // signals counts as signalling when it completes.
   launch_begin("plan_docs", s);
-  cudaError_t e = launch_k(false, k_plan_docs, dim3(1), dim3(1024), 0, s, p);
+  cudaError_t e = launch_k(true, k_plan_docs, dim3(1), dim3(1024), 0, s, p);
   launch_end("plan_docs", s);
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(4 * p.nb_cap);
