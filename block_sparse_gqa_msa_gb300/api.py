@@ -50,6 +50,7 @@ class MsaPlanStruct(ctypes.Structure):
         ("scan_tmp_len", ctypes.c_int64),
         ("item_cap", ctypes.c_int64), ("grouped", ctypes.c_void_p), ("items", ctypes.c_void_p),
         ("fflag", ctypes.c_void_p), ("fpos", ctypes.c_void_p), ("ftasks", ctypes.c_void_p),
+        ("rows", ctypes.c_void_p),
     ]
 
 

@@ -271,65 +271,71 @@ __device__ __forceinline__ float row_shift(float c2, float qnorm, float km, floa
 }
 
 // ------------------------------------------------------------ fwd_rows
-// One warp per ungrouped (token, index head): the shift M2 of each of the 16
-// heads' rows (-inf when the row sees no key), and zero the row's pool and
-// sum.  Grouped rows are the group kernel's alone.
+// One warp per ungrouped (token, index head), from the plan's list of the
+// pooled path's rows: the shift M2 of each of the 16 heads' rows (-inf when
+// the row sees no key), and zero the row's pool and sum.  Grouped rows are
+// the group kernel's alone.
 __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat16* Q,
                                                   const float* kmax, const float* vmax,
                                                   float c2, float* M2, float* lsum,
                                                   float* pool) {
   grid_dep_wait();
   grid_dep_release();
+  if (plan_failed(p.header)) return;
   const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= p.T * kKVHeads || plan_failed(p.header)) return;
-  const int64_t t = wid >> 2;
-  const int g = int(wid & 3);
-  if (p.grouped[int64_t(g) * p.T + t]) return;
-  const int d = doc_of_token(p.doc_offsets, p.num_docs, t);
-  const DocInfo di = reinterpret_cast<const DocInfo*>(p.doc_info)[d];
-  const int64_t qb = (t - di.start) / kBlock;
-  float km = -1.f, vm = 0.f;
-  if (lane < kTopK) {
-    const int32_t v = p.q2k[(int64_t(g) * p.T + t) * kTopK + lane];
-    if (v >= 0 && v <= qb) {
-      km = kmax[int64_t(g) * p.nb_cap + di.blk_base + v];
-      vm = vmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+  // a warp per entry of the plan's list of pooled rows (4 t + g)
+  const int64_t nrows = p.header[kHdrRows];
+  const int64_t nw = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t wi = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < nrows;
+       wi += nw) {
+    const int32_t ent = p.rows[wi];
+    const int64_t t = ent >> 2;
+    const int g = ent & 3;
+    const int d = doc_of_token(p.doc_offsets, p.num_docs, t);
+    const DocInfo di = reinterpret_cast<const DocInfo*>(p.doc_info)[d];
+    const int64_t qb = (t - di.start) / kBlock;
+    float km = -1.f, vm = 0.f;
+    if (lane < kTopK) {
+      const int32_t v = p.q2k[(int64_t(g) * p.T + t) * kTopK + lane];
+      if (v >= 0 && v <= qb) {
+        km = kmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+        vm = vmax[int64_t(g) * p.nb_cap + di.blk_base + v];
+      }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
-    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-  }
-  // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
-  const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-  float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-  const int half = lane >> 4, sub = lane & 15;
+    for (int o = 16; o > 0; o >>= 1) {
+      km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+    }
+    // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
+    const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
+    float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
+    const int half = lane >> 4, sub = lane & 15;
 #pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int hh = 2 * i + half;
-    const uint4 x = reinterpret_cast<const uint4*>(qrow + hh * kHeadDim)[sub];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    float s = 0.f;
+    for (int i = 0; i < 8; ++i) {
+      const int hh = 2 * i + half;
+      const uint4 x = reinterpret_cast<const uint4*>(qrow + hh * kHeadDim)[sub];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
-      s = fmaf(a, a, s);
-      s = fmaf(b, b, s);
-    }
+      for (int e = 0; e < 4; ++e) {
+        const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+        s = fmaf(a, a, s);
+        s = fmaf(b, b, s);
+      }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (sub == 0) {
-      const int64_t row = t * kQHeads + g * kHeadsPerGroup + hh;
-      M2[row] = row_shift(c2, sqrtf(s), km, vm);
-      lsum[row] = 0.f;
+      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (sub == 0) {
+        const int64_t row = t * kQHeads + g * kHeadsPerGroup + hh;
+        M2[row] = row_shift(c2, sqrtf(s), km, vm);
+        lsum[row] = 0.f;
+      }
     }
-  }
-  float4* z = reinterpret_cast<float4*>(prow);
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* z = reinterpret_cast<float4*>(prow);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
+    for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
+  }
 }
 
 // ------------------------------------------------------------ shared pieces
@@ -1331,10 +1337,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 }
 
 // ------------------------------------------------------------ fwd_finalize
-// Pooled rows: O = pool / sum -> bf16 and LSE = (M + log2 sum) ln 2.  Each
-// warp finishes eight rows per step (16 lanes x 8 elements per row; the
-// eight rows are heads of one token and index head), all loads issued before
-// any use.  Grouped rows were written by the group kernel.  Rows whose sum
+// Pooled rows (the plan's list): O = pool / sum -> bf16 and LSE =
+// (M + log2 sum) ln 2.  Each warp finishes eight rows per step (16 lanes x 8
+// elements per row; the eight rows are heads of one token and index head),
+// all loads issued before any use.  Grouped rows were written by the group
+// kernel.  Rows whose sum
 // underflowed are listed for the fallback.
 constexpr int kFinRowsPerWarp = 8;
 __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M2,
@@ -1345,13 +1352,15 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
   grid_dep_release();
   if (plan_failed(p.header)) return;
   const int lane = threadIdx.x & 31, sub = lane & 15;
-  const int64_t rows = p.T * kQHeads;
+  // the plan's list of pooled rows: entry 4 t + g is the 16 rows of token t,
+  // index head g, finished by a warp in two steps of eight
+  const int64_t nsteps = 2 * p.header[kHdrRows];
   const int64_t nwarps = int64_t(gridDim.x) * blockDim.x / 32;
-  for (int64_t r0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32 * kFinRowsPerWarp;
-       r0 < rows; r0 += nwarps * kFinRowsPerWarp) {
-    const int64_t t = r0 / kQHeads;
-    const int g = int(r0 % kQHeads) / kHeadsPerGroup;
-    if (p.grouped[int64_t(g) * p.T + t]) continue;
+  for (int64_t j = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; j < nsteps;
+       j += nwarps) {
+    const int32_t ent = p.rows[j >> 1];
+    const int64_t r0 = (int64_t(ent >> 2) * kQHeads + (ent & 3) * kHeadsPerGroup) +
+                       (j & 1) * kFinRowsPerWarp;
     float4 a[4], b[4];
     float m2[4], l[4];
 #pragma unroll
@@ -1514,9 +1523,8 @@ cudaError_t launch_forward(const msa_plan& p, const void* q, const void* k, cons
   e = launch_k(true, k_fwd_group, dim3(grid), dim3(kGrpThreads), kGrpSmem, s, prm, mQ, mK, mV);
   launch_end("fwd_group", s);
   if (e != cudaSuccess) return e;
-  const int64_t warps = p.T * kKVHeads;
   launch_begin("fwd_rows", s);
-  e = launch_k(true, k_fwd_rows, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, s, p, qb,
+  e = launch_k(true, k_fwd_rows, dim3(grid * 16), dim3(256), 0, s, p, qb,
                (const float*)kmax, (const float*)vmax, c2, M2, lsum, pool);
   launch_end("fwd_rows", s);
   if (e != cudaSuccess) return e;

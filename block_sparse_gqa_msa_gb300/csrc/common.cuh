@@ -32,6 +32,7 @@ enum HeaderSlot {
   kHdrTriPerG = 6,  // count entries per index head
   kHdrItems = 7,    // octet-group items of the forward
   kHdrFTasks = 8,   // tasks of the forward's pooled task list
+  kHdrRows = 9,     // (token, index head) pairs outside the octet groups
   kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..64)
   kHdrCostFill = 88,  // placement counters of the items, per cost
   kHdrWords = 160
@@ -129,7 +130,8 @@ __host__ __device__ __forceinline__ int64_t tri_local(int64_t n, int64_t Zs, int
 struct PlanLayout {
   int64_t nb_cap, tri_cap, nnz_cap, task_cap, item_cap, scan_tmp_len;
   size_t off_header, off_doc_info, off_doc_tri, off_cnt, off_off, off_col, off_tcnt, off_toff,
-      off_tasks, off_scan, off_grouped, off_items, off_fflag, off_fpos, off_ftasks, total;
+      off_tasks, off_scan, off_grouped, off_items, off_fflag, off_fpos, off_ftasks, off_rows,
+      total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -165,6 +167,7 @@ inline PlanLayout plan_layout(int64_t T, int32_t D) {
   L.off_fflag = o;    o = align_up(o + sizeof(int32_t) * L.task_cap, 256);
   L.off_fpos = o;     o = align_up(o + sizeof(int32_t) * L.task_cap, 256);
   L.off_ftasks = o;   o = align_up(o + sizeof(int4) * L.task_cap, 256);
+  L.off_rows = o;     o = align_up(o + sizeof(int32_t) * kKVHeads * T, 256);
   L.total = o;
   return L;
 }

@@ -282,6 +282,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
   p.fflag = reinterpret_cast<int32_t*>(w + L.off_fflag);
   p.fpos = reinterpret_cast<int32_t*>(w + L.off_fpos);
   p.ftasks = reinterpret_cast<int32_t*>(w + L.off_ftasks);
+  p.rows = reinterpret_cast<int32_t*>(w + L.off_rows);
   if (launch_plan(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MSA_ERR_CUDA;
   *out = p;
   return MSA_OK;
@@ -289,7 +290,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
 
 static msa_status check_plan(const msa_plan* plan) {
   if (!plan || plan->T < 1 || !plan->header || !plan->tasks || !plan->ftasks || !plan->items ||
-      !plan->grouped)
+      !plan->grouped || !plan->rows)
     return MSA_ERR_INVALID_ARG;
   return MSA_OK;
 }

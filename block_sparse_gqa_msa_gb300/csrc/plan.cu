@@ -340,8 +340,22 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
              (dense(2 * i) && dense(2 * i + 1));
     };
     const int o = r >> 3;
-    if (PASS == kPassCount && valid)
-      p.grouped[int64_t(g) * p.T + t] = (uniform(o) || dense(o)) ? 1 : 0;
+    if (PASS == kPassCount) {
+      const bool grp = uniform(o) || dense(o);
+      if (valid) p.grouped[int64_t(g) * p.T + t] = grp ? 1 : 0;
+      // the pooled path's rows: appended by warp, in no particular order
+      const unsigned m = __ballot_sync(0xffffffffu, valid && !grp);
+      if (m) {
+        const int lane = r & 31;
+        unsigned long long base = 0ull;
+        if (lane == 0)
+          base = atomicAdd(reinterpret_cast<unsigned long long*>(hdr + kHdrRows),
+                           (unsigned long long)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (valid && !grp)
+          p.rows[base + __popc(m & ((1u << lane) - 1u))] = int32_t(t) * kKVHeads + g;
+      }
+    }
     const bool dn = dense(o);
     if ((r & 7) == 0 && (uniform(o) || dn) && !((o & 1) && paired(o >> 1))) {
       const bool hasB = !(o & 1) && paired(o >> 1);

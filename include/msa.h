@@ -155,14 +155,19 @@ typedef struct msa_plan {
   int32_t* scan_tmp;  /* device: scan scratch                               */
   int64_t scan_tmp_len;
   /* The forward's octet groups: aligned runs of 8 tokens (document positions
-   * 8k .. 8k+7) whose tokens all see the same selected blocks; their tiles
-   * are accumulated block after block in one place, without the pool. */
+   * 8k .. 8k+7, one block b) whose tokens all see the same selected blocks,
+   * or whose block range 0 .. b is short (dense octets, each token masked to
+   * its own blocks); their tiles are accumulated block after block in one
+   * place, without the pool. */
   int64_t item_cap;   /* bound on octet-group items                        */
   uint8_t* grouped;   /* device: [4][T] 1 = the token's octet is grouped    */
   int32_t* items;     /* device: [item_cap][20] group items (msa_plan_export_groups) */
   int32_t* fflag;     /* device: [task_cap] task has an ungrouped query      */
   int32_t* fpos;      /* device: [task_cap] exclusive prefix of fflag        */
   int32_t* ftasks;    /* device: [task_cap][4] the forward's pooled tasks    */
+  int32_t* rows;      /* device: [4 T] the (token t, index head g) pairs
+                       * outside the octet groups, as 4 t + g, in no
+                       * particular order (the pooled path's rows)           */
 } msa_plan;
 
 /* Bytes of plan workspace needed for T tokens in num_docs documents.
@@ -193,7 +198,7 @@ msa_status msa_build_plan(const int32_t* q2k, const int32_t* doc_offsets, int64_
  *   - The tables live in one static 16 MiB device array that every GPU which
  *     loads the library keeps until the process exits.  A problem is
  *     accepted while msa_plan_workspace_bytes(T, num_docs) <= 16 MiB (about
- *     T <= 21600 tokens, a little more or less with the number of
+ *     T <= 21400 tokens, a little more or less with the number of
  *     documents); larger ones are rejected with MSA_ERR_WORKSPACE after the
  *     argument checks and before any CUDA call.
  *   - Each call looks the array's device address up on the current device

@@ -89,9 +89,11 @@ def test_forward_backward_host_checks(lib):
     st.T, st.num_docs = 100, 1
     st.header, st.tasks = 0x10000, 0x20000
     ref = ctypes.byref(st)
-    # a plan without its octet-group tables is rejected
+    # a plan without its octet-group tables (or its list of pooled rows) is rejected
     assert lib.msa_forward(ref, g, g, g, 0.1, g, g, g, 1 << 30, None) == 1
     st.grouped, st.items, st.ftasks = 0x30000, 0x40000, 0x50000
+    assert lib.msa_forward(ref, g, g, g, 0.1, g, g, g, 1 << 30, None) == 1
+    st.rows = 0x60000
     assert lib.msa_forward(ref, None, g, g, 0.1, g, g, g, 1 << 30, None) == 1
     assert lib.msa_forward(ref, g, g, g, -1.0, g, g, g, 1 << 30, None) == 1
     assert lib.msa_forward(ref, ctypes.c_void_p(0x10008), g, g, 0.1, g, g, g, 1 << 30, None) == 3
