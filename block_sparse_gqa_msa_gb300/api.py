@@ -180,7 +180,7 @@ def msa_build_plan(q2k: torch.Tensor, doc_offsets: torch.Tensor, super_block: in
     o_accum: precision of the forward's O pool (only "f32" is accepted; the
     library rejects "bf16", whose O error exceeds the forward's bar);
     dense_blocks: bound on the query block (b + 1 <= dense_blocks) of the
-    forward's dense octets (0: the default, 28; -1: none)."""
+    forward's dense octets (0: the default, 32; -1: none)."""
     if q2k.dim() != 3:
         raise ValueError("q2k must be [4, T, 16]")
     T = int(q2k.shape[1])
@@ -296,12 +296,12 @@ def msa_plan_export(plan: Plan, stream=None):
 
 
 def msa_plan_export_groups(plan: Plan, stream=None):
-    """(grouped uint8 [4, T], items int32 [n_items, 20], ftasks int32
+    """(grouped uint8 [4, T], items int32 [n_items, 36], ftasks int32
     [n_ftasks, 4]) - the forward's octet groups - copied to host."""
     cnt = msa_plan_counts(plan, stream)
     T = plan.struct.T
     grouped = np.zeros((4, T), dtype=np.uint8)
-    items = np.zeros((max(cnt["items"], 1), 20), dtype=np.int32)
+    items = np.zeros((max(cnt["items"], 1), 36), dtype=np.int32)
     ftasks = np.zeros((max(cnt["ftasks"], 1), 4), dtype=np.int32)
     _check(lib().msa_plan_export_groups(plan.ref(), _stream(stream), grouped.ctypes.data_as(_P),
                                         T, items.ctypes.data_as(_P), items.shape[0],

@@ -1228,12 +1228,14 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       const int32_t tok = tok0 + (qi < nq ? qi : nq - 1);
       const int32_t dstart = dinfo[iv.doc].start;
       // dense item: the row's token takes part in block j where bit j is set
-      const uint32_t tmask = iv.dense ? uint32_t(it[4 + 8 * x + qi]) : ~0u;
+      const int tw = 4 + 2 * (8 * x + qi);
+      const uint64_t tmask =
+          iv.dense ? (uint64_t(uint32_t(it[tw])) | uint64_t(uint32_t(it[tw + 1])) << 32) : ~0ull;
       float mref = -INFINITY, lsum = 0.f;
       bool ok = true;
       for (int j = 0; j < iv.nsel; ++j) {
         const int32_t key_start = dstart + (iv.dense ? j : it[4 + j]) * kBlock;
-        const int jmax = qi < nq && ((tmask >> j) & 1u) ? min(tok - key_start, kBlock - 1) : -1;
+        const int jmax = qi < nq && ((tmask >> j) & 1ull) ? min(tok - key_start, kBlock - 1) : -1;
         // S_x(j) complete: so is P_x(j-1) . V, which was issued before it
         if (!mbar_wait_warp(smem_u32(&bars.s_full[x]), uint32_t(nx & 1), abort_flag)) {
           ok = false;

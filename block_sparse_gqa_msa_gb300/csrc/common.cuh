@@ -33,13 +33,13 @@ enum HeaderSlot {
   kHdrItems = 7,    // octet-group items of the forward
   kHdrFTasks = 8,   // tasks of the forward's pooled task list
   kHdrRows = 9,     // (token, index head) pairs outside the octet groups
-  kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..64)
-  kHdrCostFill = 88,  // placement counters of the items, per cost
-  kHdrWords = 160
+  kHdrCost = 16,    // [kHdrCost + c]: items of cost c (1..128)
+  kHdrCostFill = 145,  // placement counters of the items, per cost
+  kHdrWords = 288
 };
-constexpr int kMaxDenseBlocks = 32;   // a dense octet's token masks are 32-bit words
-constexpr int kDefaultDenseBlocks = 28;
-constexpr int kMaxItemCost = 2 * kMaxDenseBlocks;  // an item: at most 2 octets x 32 blocks
+constexpr int kMaxDenseBlocks = 64;   // a dense octet's token masks are 64-bit words
+constexpr int kDefaultDenseBlocks = 32;
+constexpr int kMaxItemCost = 2 * kMaxDenseBlocks;  // an item: at most 2 octets x 64 blocks
 
 __device__ __forceinline__ void raise_status(int64_t* header, msa_status s) {
   atomicOr(reinterpret_cast<unsigned long long*>(header + kHdrStatus),
@@ -85,11 +85,12 @@ __device__ __forceinline__ TaskView decode_task(int4 t) {
 //   [2] queries of A | queries of B << 4 | index head << 8 | blocks << 12 |
 //       dense << 20,
 //   [3] document index,
-//   [4 .. 20) uniform item (all tokens see the same blocks): the blocks
-//       (document-local, ascending, -1 padded); dense item (blocks 0 .. b,
-//       b + 1 = the block count): per token of A then of B, the mask of the
-//       blocks it selected (bit v; 0 past the octet's end).
-constexpr int kItemWords = 20;
+//   [4 .. 36) uniform item (all tokens see the same blocks): the blocks
+//       (document-local, ascending, -1 padded) in [4, 20); dense item
+//       (blocks 0 .. b, b + 1 = the block count): per token of A then of B,
+//       the 64-bit mask of the blocks it selected (bit v; low word first; 0
+//       past the octet's end).
+constexpr int kItemWords = 36;
 struct ItemView {
   int32_t tokA, tokB, nqA, nqB, g, nsel, doc;
   bool dense;
@@ -102,7 +103,7 @@ __device__ __forceinline__ ItemView decode_item(const int32_t* it) {
   v.nqA = h.z & 0xF;
   v.nqB = (h.z >> 4) & 0xF;
   v.g = (h.z >> 8) & 0x3;
-  v.nsel = (h.z >> 12) & 0x3F;
+  v.nsel = (h.z >> 12) & 0x7F;
   v.dense = (h.z >> 20) & 1;
   v.doc = h.w;
   return v;

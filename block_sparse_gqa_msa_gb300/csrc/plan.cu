@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
   __shared__ unsigned long long s_pairs;
   __shared__ int s_nsel[16];        // per octet: blocks selected by any of its queries
   __shared__ uint32_t s_bad, s_pdiff;  // octets not uniform; pairs with different sets
-  __shared__ uint32_t s_mask[128];     // dense octets: each query's block mask
+  __shared__ uint64_t s_mask[128];     // dense octets: each query's block mask
   __shared__ int64_t s_hist[kMaxItemCost + 1];  // items per cost
   int64_t* hdr = p.header;
   const int64_t NB = hdr[kHdrNB];
@@ -317,13 +317,14 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
     // dense octets: this query's visible selected blocks as a bit mask
     const bool dense_ok = qb + 1 <= p.dense_blocks;
     // items per cost (complete after the count pass), for the placements
-    if (PASS == kPassScatter && threadIdx.x <= kMaxItemCost)
-      s_hist[threadIdx.x] = threadIdx.x == 0 ? 0 : hdr[kHdrCost + threadIdx.x];
+    if (PASS == kPassScatter)
+      for (int c = threadIdx.x; c <= kMaxItemCost; c += blockDim.x)
+        s_hist[c] = c == 0 ? 0 : hdr[kHdrCost + c];
     if (PASS == kPassScatter && dense_ok) {
-      uint32_t m = 0u;
+      uint64_t m = 0ull;
 #pragma unroll
       for (int i = 0; i < kTopK; ++i)
-        if (sl[i] >= 0 && sl[i] <= qb) m |= 1u << sl[i];
+        if (sl[i] >= 0 && sl[i] <= qb) m |= 1ull << sl[i];
       s_mask[r] = m;
     }
     __syncthreads();
@@ -380,7 +381,9 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const int oo = o + (k >> 3), qi = k & 7;
-            it[4 + k] = (k < 8 || hasB) && qi < octet_rows(oo) ? int32_t(s_mask[8 * oo + qi]) : 0;
+            const uint64_t m = (k < 8 || hasB) && qi < octet_rows(oo) ? s_mask[8 * oo + qi] : 0ull;
+            it[4 + 2 * k] = int32_t(uint32_t(m));
+            it[5 + 2 * k] = int32_t(uint32_t(m >> 32));
           }
         } else {
           // this query's visible blocks (distinct after the dedupe), ascending

@@ -109,7 +109,7 @@ typedef struct msa_plan_options {
    * b whose tokens see different blocks runs as one tile over all blocks
    * 0 .. b, each token's rows masked to its own blocks, when b + 1 <=
    * dense_blocks (instead of through the pooled tasks).  0 selects the
-   * default, 28; -1 turns dense octets off; 1 .. 32 set the bound; other
+   * default, 32; -1 turns dense octets off; 1 .. 64 set the bound; other
    * values give MSA_ERR_INVALID_ARG. */
   int32_t dense_blocks;
   int32_t reserved[4];
@@ -161,7 +161,7 @@ typedef struct msa_plan {
    * place, without the pool. */
   int64_t item_cap;   /* bound on octet-group items                        */
   uint8_t* grouped;   /* device: [4][T] 1 = the token's octet is grouped    */
-  int32_t* items;     /* device: [item_cap][20] group items (msa_plan_export_groups) */
+  int32_t* items;     /* device: [item_cap][36] group items (msa_plan_export_groups) */
   int32_t* fflag;     /* device: [task_cap] task has an ungrouped query      */
   int32_t* fpos;      /* device: [task_cap] exclusive prefix of fflag        */
   int32_t* ftasks;    /* device: [task_cap][4] the forward's pooled tasks    */
@@ -272,10 +272,13 @@ msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* c
  * Copy the forward's octet-group tables to host memory after synchronising
  * the stream (for the plan tests).  Each destination may be NULL to skip it.
  *   grouped uint8 [4][T]: 1 where the token's octet is grouped
- *   items   int32 [n_items][20]: first token of octet A, of octet B (-1 if
- *           none), queries of A | of B << 4 | index head << 8 | blocks << 12,
- *           document index, then the blocks ascending (-1 padded); items are
- *           ordered by decreasing work (blocks x octets)
+ *   items   int32 [n_items][36]: first token of octet A, of octet B (-1 if
+ *           none), queries of A | of B << 4 | index head << 8 | blocks << 12
+ *           | dense << 20, document index, then for a uniform item the
+ *           blocks ascending (-1 padded, 16 words), for a dense one (blocks
+ *           0 .. b) each token's 64-bit block mask as a low and a high word
+ *           (tokens of A, then of B; 32 words); items are ordered by
+ *           decreasing work (blocks x octets)
  *   ftasks  int32 [n_ftasks][4]: the task records (as in msa_plan_export) of
  *           the tasks with at least one ungrouped query, in task order
  * Capacities are element counts of the first dimension (T for grouped, which

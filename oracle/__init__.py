@@ -246,7 +246,7 @@ def plan(q2k, doc_offsets, T: int, super_block: int = 16, lib=None):
     }
 
 
-DENSE_BLOCKS = 28
+DENSE_BLOCKS = 32
 
 
 def groups(q2k, doc_offsets, T: int, dense_blocks: int = DENSE_BLOCKS, lib=None):

@@ -542,7 +542,7 @@ int oracle_threads(void) {
  *            tokA .. tokA+7 and tokB .. tokB+7 (0 past the octet's end);
  *            nsel = |S| (uniform) or b + 1 (dense); items in (g, d, k) order
  *   counts:  [0] = items
- * dense_blocks <= 0 makes no octet dense; it is at most 32 (one 32-bit mask
+ * dense_blocks <= 0 makes no octet dense; it is at most 64 (one 64-bit mask
  * per token).  The forward's task list is then the task list without the
  * tasks all of whose queries are grouped (see oracle/__init__.py).
  */
@@ -552,7 +552,7 @@ enum { OCT_NONE = 0, OCT_UNIFORM = 1, OCT_DENSE = 2 };
 int oracle_groups(const int32_t* q2k, int64_t T, const int32_t* offs, int32_t D,
                   int32_t dense_blocks, unsigned char* grouped, int64_t* items,
                   int64_t item_cap, int64_t* counts) {
-  if (T <= 0 || check_offsets(offs, D, T) || dense_blocks > 32) return OR_BAD_ARGS;
+  if (T <= 0 || check_offsets(offs, D, T) || dense_blocks > 64) return OR_BAD_ARGS;
   if (check_q2k(q2k, T, offs, D)) return OR_BAD_Q2K;
   int32_t maxnb = 0;
   for (int32_t d = 0; d < D; ++d)

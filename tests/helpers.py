@@ -79,12 +79,16 @@ def canonical_items(items, gpu):
         r = [int(x) for x in r]
         if gpu:
             z = r[2]
-            key = (z >> 8 & 3, r[0], r[1], z & 0xF, z >> 4 & 0xF, z >> 12 & 0x3F, z >> 20 & 1)
-            words = r[4:20]
+            key = (z >> 8 & 3, r[0], r[1], z & 0xF, z >> 4 & 0xF, z >> 12 & 0x7F, z >> 20 & 1)
+            if key[6]:  # dense: 16 64-bit masks as (low, high) word pairs
+                words = [(r[4 + 2 * k] & 0xFFFFFFFF) | (r[5 + 2 * k] & 0xFFFFFFFF) << 32
+                         for k in range(16)]
+            else:
+                words = r[4:20]
         else:
             key = (r[4], r[0], r[1], r[2], r[3], r[5], r[6])
             words = r[7:23]
-        if key[6]:  # dense: 32-bit masks, unsigned
-            words = [w & 0xFFFFFFFF for w in words]
+            if key[6]:
+                words = [w & 0xFFFFFFFFFFFFFFFF for w in words]
         out.append(key + tuple(words))
     return sorted(out)

@@ -62,7 +62,7 @@ def _check(lens, q2k, Z, dense=0):
     assert np.array_equal(grouped, og["grouped"])
     assert counts["items"] == len(og["items"])
     assert canonical_items(items, True) == canonical_items(og["items"], False)
-    cost = (items[:, 2] >> 12 & 0x3F) * np.where(items[:, 1] >= 0, 2, 1)
+    cost = (items[:, 2] >> 12 & 0x7F) * np.where(items[:, 1] >= 0, 2, 1)
     assert (np.diff(cost) <= 0).all()
     oft = oracle.forward_tasks(pl, og["grouped"])
     assert counts["ftasks"] == len(oft)
@@ -83,7 +83,7 @@ def test_plan_bit_exact(name, Z):
 
 
 @pytest.mark.parametrize("name", ["cfg3", "irregular", "long-doc"])
-@pytest.mark.parametrize("dense", [-1, 3, 32])
+@pytest.mark.parametrize("dense", [-1, 3, 64])
 def test_plan_dense_bounds(name, dense):
     # dense octets off, a small bound, and the largest one
     lens, q2k = STRUCTURES[name]()
