@@ -738,77 +738,130 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------ bwd_finalize
-// Pools -> bf16 outputs.  dQ: one thread per (head octet of a token, 8 head
-// dimensions) reads the 64 interleaved pool values and writes 8 dims of each
-// of the octet's heads; dK / dV: 8 elements per thread.  A non-finite value
-// in a 16-bit dQ pool (fp16 saturates above 65504) sets MSA_ERR_RANGE.
-__global__ void __launch_bounds__(256) k_bwd_finalize(msa_plan p, const void* dq_pool,
-                                                      const float* dk_pool, const float* dv_pool,
-                                                      __nv_bfloat16* dq, __nv_bfloat16* dk,
-                                                      __nv_bfloat16* dv) {
+// Pools -> bf16 outputs.  A 16-bit dQ pool (fp16 default, bf16) is taken a
+// head octet of a token at a time: the octet's 2 KB ([128 d][8 heads]) is
+// read by one warp, 512 contiguous bytes per instruction, converted and
+// transposed through shared memory to [8 heads][128 d], and written back as
+// 512 contiguous bytes per instruction.  An fp32 pool: one thread per
+// (head octet, 8 head dimensions).  dK / dV: 8 elements per thread.  A
+// non-finite value in an fp16 pool (fp16 saturates above 65504) sets
+// MSA_ERR_RANGE.
+constexpr int kFinThreads = 256;
+constexpr int kFinOcts = 2;  // head octets per warp iteration (loads in flight)
+template <int ACC>
+__global__ void __launch_bounds__(kFinThreads) k_bwd_finalize(msa_plan p, const void* dq_pool,
+                                                              const float* dk_pool,
+                                                              const float* dv_pool,
+                                                              __nv_bfloat16* dq,
+                                                              __nv_bfloat16* dk,
+                                                              __nv_bfloat16* dv) {
+  // per warp: kFinOcts octets of [8 heads][128 d] bf16
+  __shared__ __align__(16) uint16_t stage[kFinThreads / 32][kFinOcts][8][kHeadDim];
   grid_dep_wait();
   grid_dep_release();
   if (plan_failed(p.header)) return;
-  const int64_t nq = p.T * (kQHeads / 8) * (kHeadDim / 8);
+  const int lane = threadIdx.x & 31;
+  const int64_t n_oct = p.T * (kQHeads / 8);
   const int64_t nk8 = p.T * kKVHeads * kHeadDim / 8;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   uint32_t nonfinite = 0u;  // OR of the exponent fields that were all ones
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq + 2 * nk8;
-       i += stride) {
-    if (i < nq) {
+  if (ACC != MSA_DQ_ACCUM_F32) {
+    constexpr bool f16 = ACC == MSA_DQ_ACCUM_F16;
+    uint16_t (*st)[8][kHeadDim] = stage[threadIdx.x >> 5];
+    const uint4* src = static_cast<const uint4*>(dq_pool);  // [oct][d][8 heads]
+    const int64_t nwarps = stride >> 5;
+    for (int64_t u = tid >> 5; u * kFinOcts < n_oct; u += nwarps) {
+      uint4 w[kFinOcts][4];
+#pragma unroll
+      for (int o = 0; o < kFinOcts; ++o) {
+        const int64_t oct = u * kFinOcts + o;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          w[o][k] = oct < n_oct ? src[oct * kHeadDim + 32 * k + lane] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int o = 0; o < kFinOcts; ++o) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ws[4] = {w[o][k].x, w[o][k].y, w[o][k].z, w[o][k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // heads 2j (low half), 2j + 1 (high half)
+            uint32_t b2;
+            if (f16) {
+              b2 = pack_bf16x2(f16_lo(ws[j]), f16_hi(ws[j]));
+              nonfinite |= ((ws[j] & 0x7C00u) == 0x7C00u) |
+                           ((ws[j] & 0x7C000000u) == 0x7C000000u);
+            } else {
+              b2 = ws[j];  // bf16 pool: already the output type
+            }
+            st[o][2 * j][32 * k + lane] = uint16_t(b2 & 0xFFFFu);
+            st[o][2 * j + 1][32 * k + lane] = uint16_t(b2 >> 16);
+          }
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int o = 0; o < kFinOcts; ++o) {
+        const int64_t oct = u * kFinOcts + o;
+        if (oct < n_oct) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {  // lanes 0-15: head 2r, lanes 16-31: head 2r + 1
+            const int h = 2 * r + (lane >> 4);
+            const uint4 v = reinterpret_cast<const uint4*>(st[o][h])[lane & 15];
+            reinterpret_cast<uint4*>(dq + (oct * 8 + h) * kHeadDim)[lane & 15] = v;
+          }
+        }
+      }
+      __syncwarp();
+      // the octets' pool lines (16 each) are dead: drop them from L2
+#pragma unroll
+      for (int o = 0; o < kFinOcts; o += 2) {
+        const int64_t oct = u * kFinOcts + o + (lane >> 4);
+        if (oct < n_oct) l2_discard_line(src + oct * kHeadDim + 8 * (lane & 15));
+      }
+    }
+  } else {
+    const int64_t nq = n_oct * (kHeadDim / 8);
+    for (int64_t i = tid; i < nq; i += stride) {
       const int64_t oct = i >> 4;  // token * 8 + head octet
       const int d0 = int(i & 15) * 8;
       uint32_t out[8][4];  // [head in octet][dims pair]
-      if (p.dq_accum == MSA_DQ_ACCUM_F32) {
-        const float4* src = reinterpret_cast<const float4*>(
-            static_cast<const float*>(dq_pool) + (oct * kHeadDim + d0) * 8);
+      const float4* src = reinterpret_cast<const float4*>(
+          static_cast<const float*>(dq_pool) + (oct * kHeadDim + d0) * 8);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {  // dims d0 + e, d0 + e + 1
-          const float4 a0 = src[2 * e], a1 = src[2 * e + 1];
-          const float4 b0 = src[2 * e + 2], b1 = src[2 * e + 3];
-          const float fa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          const float fb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      for (int e = 0; e < 8; e += 2) {  // dims d0 + e, d0 + e + 1
+        const float4 a0 = src[2 * e], a1 = src[2 * e + 1];
+        const float4 b0 = src[2 * e + 2], b1 = src[2 * e + 3];
+        const float fa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float fb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-          for (int h = 0; h < 8; ++h) out[h][e / 2] = pack_bf16x2(fa[h], fb[h]);
-        }
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(dq_pool) + (oct * kHeadDim + d0) * 8);
-        const bool f16 = p.dq_accum == MSA_DQ_ACCUM_F16;
-        auto val = [&](uint32_t w, bool hi) {
-          return f16 ? (hi ? f16_hi(w) : f16_lo(w)) : (hi ? bf16_hi(w) : bf16_lo(w));
-        };
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const uint4 a = src[e], b = src[e + 1];
-          const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int h = 0; h < 8; ++h)
-            out[h][e / 2] = pack_bf16x2(val(wa[h >> 1], h & 1), val(wb[h >> 1], h & 1));
-          if (f16) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              nonfinite |= ((wa[k] & 0x7C00u) == 0x7C00u) | ((wa[k] & 0x7C000000u) == 0x7C000000u);
-              nonfinite |= ((wb[k] & 0x7C00u) == 0x7C00u) | ((wb[k] & 0x7C000000u) == 0x7C000000u);
-            }
-          }
-        }
+        for (int h = 0; h < 8; ++h) out[h][e / 2] = pack_bf16x2(fa[h], fb[h]);
       }
 #pragma unroll
       for (int h = 0; h < 8; ++h)
         *reinterpret_cast<uint4*>(dq + (oct * 8 + h) * kHeadDim + d0) =
             make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
-    } else {
-      const int64_t j = i < nq + nk8 ? i - nq : i - nq - nk8;
-      const float* src = i < nq + nk8 ? dk_pool : dv_pool;
-      const float4 a = reinterpret_cast<const float4*>(src)[2 * j];
-      const float4 b = reinterpret_cast<const float4*>(src)[2 * j + 1];
-      *(reinterpret_cast<uint4*>(i < nq + nk8 ? dk : dv) + j) =
-          make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                     pack_bf16x2(b.z, b.w));
     }
   }
-  if (__any_sync(0xffffffffu, nonfinite != 0u) && (threadIdx.x & 31) == 0)
+  // dK / dV: a thread per 128-byte pool line (32 elements), dropped from L2
+  // once read
+  const int64_t nk32 = nk8 / 4;
+  for (int64_t i = tid; i < 2 * nk32; i += stride) {
+    const int64_t j = i < nk32 ? i : i - nk32;
+    const float4* src = reinterpret_cast<const float4*>(i < nk32 ? dk_pool : dv_pool) + 8 * j;
+    float4 a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] = src[e];
+    uint4* dst = reinterpret_cast<uint4*>(i < nk32 ? dk : dv) + 4 * j;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      dst[e] = make_uint4(pack_bf16x2(a[2 * e].x, a[2 * e].y), pack_bf16x2(a[2 * e].z, a[2 * e].w),
+                          pack_bf16x2(a[2 * e + 1].x, a[2 * e + 1].y),
+                          pack_bf16x2(a[2 * e + 1].z, a[2 * e + 1].w));
+    l2_discard_line(src);
+  }
+  if (__any_sync(0xffffffffu, nonfinite != 0u) && lane == 0)
     raise_status(p.header, MSA_ERR_RANGE);
 }
 
@@ -872,7 +925,10 @@ cudaError_t launch_backward(const msa_plan& p, const void* q, const void* k, con
   launch_end("bwd_main", s);
   if (e != cudaSuccess) return e;
   launch_begin("bwd_finalize", s);
-  e = launch_k(true, k_bwd_finalize, dim3(grid * 8), dim3(256), 0, s, p, (const void*)dq_pool,
+  auto fin_fn = p.dq_accum == MSA_DQ_ACCUM_F32    ? k_bwd_finalize<MSA_DQ_ACCUM_F32>
+                : p.dq_accum == MSA_DQ_ACCUM_BF16 ? k_bwd_finalize<MSA_DQ_ACCUM_BF16>
+                                                  : k_bwd_finalize<MSA_DQ_ACCUM_F16>;
+  e = launch_k(true, fin_fn, dim3(grid * 4), dim3(kFinThreads), 0, s, p, (const void*)dq_pool,
                (const float*)dk_pool, (const float*)dv_pool, static_cast<__nv_bfloat16*>(dq),
                static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
   launch_end("bwd_finalize", s);

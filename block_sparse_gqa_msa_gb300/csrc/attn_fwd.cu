@@ -291,6 +291,20 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
     const int32_t ent = p.rows[wi];
     const int64_t t = ent >> 2;
     const int g = ent & 3;
+    // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head
+    // 2i+1.  The Q loads and the pool's zeroing go out first; the lookups of
+    // the row's blocks (document, q2k, kmax) run while they are in flight.
+    const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
+    float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
+    const int half = lane >> 4, sub = lane & 15;
+    uint4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      x[i] = reinterpret_cast<const uint4*>(qrow + (2 * i + half) * kHeadDim)[sub];
+    float4* z = reinterpret_cast<float4*>(prow);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
     const int d = doc_of_token(p.doc_offsets, p.num_docs, t);
     const DocInfo di = reinterpret_cast<const DocInfo*>(p.doc_info)[d];
     const int64_t qb = (t - di.start) / kBlock;
@@ -307,15 +321,10 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
       km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
     }
-    // 16 heads x 128 dims = 4 KB of Q: lanes 0-15 take head 2i, 16-31 head 2i+1.
-    const __nv_bfloat16* qrow = Q + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-    float* prow = pool + (t * kQHeads + g * kHeadsPerGroup) * kHeadDim;
-    const int half = lane >> 4, sub = lane & 15;
-#pragma unroll 2
+#pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int hh = 2 * i + half;
-      const uint4 x = reinterpret_cast<const uint4*>(qrow + hh * kHeadDim)[sub];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -331,10 +340,6 @@ __global__ void __launch_bounds__(256) k_fwd_rows(msa_plan p, const __nv_bfloat1
         lsum[row] = 0.f;
       }
     }
-    float4* z = reinterpret_cast<float4*>(prow);
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = lane; i < kHeadsPerGroup * kHeadDim / 4; i += 32) z[i] = zero;
   }
 }
 
@@ -1394,6 +1399,14 @@ __global__ void __launch_bounds__(256) k_fwd_finalize(msa_plan p, const float* M
       }
       reinterpret_cast<uint4*>(O + row * kHeadDim)[sub] = out;
       if (sub == 0) lse[row] = L;
+    }
+    // the eight rows' pool lines are dead (the fallback does not read the
+    // pool): drop them from L2, a lane per 128-byte line
+    __syncwarp();
+    if ((sub & 3) == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        l2_discard_line(pool + (r0 + 2 * i + (lane >> 4)) * kHeadDim + 8 * sub);
     }
   }
 }

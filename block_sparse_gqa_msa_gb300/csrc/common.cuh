@@ -86,7 +86,7 @@ __device__ __forceinline__ TaskView decode_task(int4 t) {
 //       dense << 20,
 //   [3] document index,
 //   [4 .. 36) uniform item (all tokens see the same blocks): the blocks
-//       (document-local, ascending, -1 padded) in [4, 20); dense item
+//       (document-local, ascending), then -1 to the end; dense item
 //       (blocks 0 .. b, b + 1 = the block count): per token of A then of B,
 //       the 64-bit mask of the blocks it selected (bit v; low word first; 0
 //       past the octet's end).

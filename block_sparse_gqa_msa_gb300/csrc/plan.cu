@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(128, 6) k_plan_blocks(msa_plan p) {
             it[4 + rank] = sl[i];
             ++nb;
           }
-          for (int k = nb; k < kTopK; ++k) it[4 + k] = -1;
+          for (int k = nb; k < kItemWords - 4; ++k) it[4 + k] = -1;  // the whole payload
         }
       }
     }

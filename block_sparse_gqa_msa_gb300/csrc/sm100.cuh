@@ -404,6 +404,16 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Drop the 128-byte line at a (128-byte aligned) from L2 without writing it
+// back: its contents become undefined.  For workspace lines whose last reader
+// is done (a pool read by its finalize and zeroed again before its next use),
+// so that dirty lines of dead data cost no DRAM writes.  The caller orders it
+// after every read of the line (same thread, or a warp barrier after the
+// reads' values were used).
+__device__ __forceinline__ void l2_discard_line(const void* a) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

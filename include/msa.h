@@ -275,7 +275,7 @@ msa_status msa_plan_export(const msa_plan* plan, msa_stream_t stream, int32_t* c
  *   items   int32 [n_items][36]: first token of octet A, of octet B (-1 if
  *           none), queries of A | of B << 4 | index head << 8 | blocks << 12
  *           | dense << 20, document index, then for a uniform item the
- *           blocks ascending (-1 padded, 16 words), for a dense one (blocks
+ *           blocks ascending, -1 padded to 32 words, for a dense one (blocks
  *           0 .. b) each token's 64-bit block mask as a low and a high word
  *           (tokens of A, then of B; 32 words); items are ordered by
  *           decreasing work (blocks x octets)

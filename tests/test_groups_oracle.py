@@ -113,7 +113,7 @@ def test_hand_worked_groups_no_dense(oracle_mod):
 def test_hand_worked_groups_dense(oracle_mod):
     lens, T, q2k = _hand_case()
     offs = inputs.offsets_from_lengths(lens)
-    gr = oracle_mod.groups(q2k, offs, T)      # default bound: 28 blocks
+    gr = oracle_mod.groups(q2k, offs, T)      # default bound: 32 blocks
     assert gr["grouped"].all()
     items = _items_by_start(gr)
     # each difference splits its pair into a uniform single and a dense
