@@ -309,15 +309,18 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- streaming kernels
-def streaming_bytes(T: int, n_ungrouped: int, dq_esz: int = 2) -> dict:
+def streaming_bytes(T: int, n_ungrouped: int, NB: int, dq_esz: int = 2) -> dict:
     """Algorithmic bytes per launch of the HBM-bound kernels: what each must
     read and write by its definition (n_ungrouped: (token, index head) pairs
-    whose octet is not grouped; dq_esz: bytes per dQ pool element)."""
+    whose octet is not grouped; NB: key blocks; dq_esz: bytes per dQ pool
+    element)."""
     kv = T * 4 * 128 * 2  # one of K, V as bf16
     rows_q = T * 64 * 128 * 2  # one of Q, O, dO as bf16
     return {
-        "fwd_kmax": 2 * kv,                                  # K, V read
-        "fwd_v16": 2 * kv,                                   # V read, fp16 V written
+        "fwd_kmax": 3 * kv + 2 * 4 * NB * 4,                 # K, V read; fp16 V, maxima written
+        "fwd_v16": 4 * NB * 4 + 4 * 4,                       # max |v| read, scales written (the
+                                                             # copy is rewritten only if a head
+                                                             # needs a scale: not here)
         "fwd_rows": n_ungrouped * (4096 + 64 + 128 + 8192),  # Q, q2k read; shifts, sums, pool zeroed
         "fwd_finalize": n_ungrouped * (8192 + 128 + 4096 + 64),  # pool, shifts, sums read; O, LSE
         "bwd_delta": 2 * rows_q + T * 64 * 4 + T * 64 * 128 * dq_esz + 2 * T * 512 * 4,
@@ -539,7 +542,7 @@ def run_gpu(args, rank, world):
             100.0 * adjacent["single_doc_16k"]["TFLOP_s"] / float(peaks["bf16_tflops"]))
     # HBM-bound kernels: algorithmic bytes per launch against the copy bandwidth
     grouped, _, _ = api.msa_plan_export_groups(plan)
-    sbytes = streaming_bytes(T, int((grouped == 0).sum()))
+    sbytes = streaming_bytes(T, int((grouped == 0).sum()), int(api.msa_plan_counts(plan)["NB"]))
     streaming = {}
     for name, nbytes in sbytes.items():
         if name in kern:
