@@ -743,11 +743,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // read by one warp, 512 contiguous bytes per instruction, converted and
 // transposed through shared memory to [8 heads][128 d], and written back as
 // 512 contiguous bytes per instruction.  An fp32 pool: one thread per
-// (head octet, 8 head dimensions).  dK / dV: 8 elements per thread.  A
-// non-finite value in an fp16 pool (fp16 saturates above 65504) sets
-// MSA_ERR_RANGE.
+// (head octet, 8 head dimensions).  dK / dV: one 128-byte pool line (32
+// elements) per thread.  Pool lines of the 16-bit dQ pool and of the dK / dV
+// pools are dropped from L2 once read (the pools are zeroed again before
+// their next use).  A non-finite value in an fp16 pool (fp16 saturates above
+// 65504) sets MSA_ERR_RANGE.
 constexpr int kFinThreads = 256;
 constexpr int kFinOcts = 2;  // head octets per warp iteration (loads in flight)
+static_assert(kFinOcts % 2 == 0, "the discard loop gives each half-warp one octet");
 template <int ACC>
 __global__ void __launch_bounds__(kFinThreads) k_bwd_finalize(msa_plan p, const void* dq_pool,
                                                               const float* dk_pool,
