@@ -66,16 +66,20 @@ def test_build_plan_host_checks(lib):
     for bad_opts in (api.MsaPlanOptions(super_block=-1),
                      api.MsaPlanOptions(super_block=16, dq_accum=3),
                      api.MsaPlanOptions(super_block=16, o_accum=2),
-                     api.MsaPlanOptions(super_block=16, o_accum=-1)):
+                     api.MsaPlanOptions(super_block=16, o_accum=-1),
+                     api.MsaPlanOptions(super_block=16, dense_blocks=-2),
+                     api.MsaPlanOptions(super_block=16, dense_blocks=65)):
         assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(bad_opts), good, ws_n.value,
                                   None, ctypes.byref(st)) == 1
     # the bf16 O pool is not offered
     assert lib.msa_build_plan(good, good, 1000, 2,
                               ctypes.byref(api.MsaPlanOptions(super_block=16, o_accum=1)), good,
                               ws_n.value, None, ctypes.byref(st)) == 2
-    # alignment
-    assert lib.msa_build_plan(ctypes.c_void_p(0x10004), good, 1000, 2, ctypes.byref(opts), good,
-                              ws_n.value, None, ctypes.byref(st)) == 3
+    # alignment (the dense bounds -1 and 64 pass the option checks and reach it)
+    for o in (opts, api.MsaPlanOptions(super_block=16, dense_blocks=-1),
+              api.MsaPlanOptions(super_block=16, dense_blocks=64)):
+        assert lib.msa_build_plan(ctypes.c_void_p(0x10004), good, 1000, 2, ctypes.byref(o), good,
+                                  ws_n.value, None, ctypes.byref(st)) == 3
     # workspace too small
     assert lib.msa_build_plan(good, good, 1000, 2, ctypes.byref(opts), good, ws_n.value - 1, None,
                               ctypes.byref(st)) == 4
