@@ -12,7 +12,10 @@ same set.
     out in the comments, once with dense octets off (the differences leave
     their octets to the pooled tasks), once with the default bound (they
     become dense items with the masks written out below) and once with a
-    bound of 2 blocks (only the difference in block 1 is dense).
+    bound of 2 blocks (only the difference in block 1 is dense);
+  * one 40-block document whose octets are all uniform but one, in block 33:
+    it is dense only with a bound of at least 34 blocks, and its token masks
+    reach past bit 31 (the high word of the 64-bit masks).
 """
 import numpy as np
 
@@ -157,3 +160,46 @@ def test_hand_worked_groups_bound(oracle_mod):
         (0, tuple(range(256, 264))),
         (0, tuple(range(256, 264))),
         (0, (256, 257, 258, 259, 261, 262, 263, 264))])
+
+
+def _long_document_case():
+    # one document of 40 blocks; a token of block b < 16 selects blocks 0 .. b,
+    # one of block b >= 16 selects 0 .. 7 and b - 7 .. b (16 blocks), so every
+    # octet is uniform; then token 4227 (block 33, octet 528) of g=0 selects
+    # 0 .. 7 and 25 .. 32 instead (block 25 in, block 33 out)
+    T = 40 * 128
+    q2k = np.full((4, T, 16), -1, dtype=np.int32)
+    for t in range(T):
+        b = t // 128
+        q2k[:, t, :] = (np.arange(b + 1).tolist() + [-1] * 16)[:16] if b < 16 else \
+            list(range(8)) + list(range(b - 7, b + 1))
+    q2k[0, 4227, :] = list(range(8)) + list(range(25, 33))
+    return [T], T, q2k
+
+
+def test_dense_mask_high_word_and_bound(oracle_mod):
+    lens, T, q2k = _long_document_case()
+    offs = inputs.offsets_from_lengths(lens)
+    usual = sum(1 << v for v in list(range(8)) + list(range(26, 34)))
+    odd = sum(1 << v for v in list(range(8)) + list(range(25, 33)))
+    # b + 1 = 34 blocks: dense only with a bound of at least 34
+    for bound, dense in ((32, False), (33, False), (34, True), (64, True)):
+        gr = oracle_mod.groups(q2k, offs, T, dense_blocks=bound)
+        g_ = gr["grouped"]
+        expect = np.ones((4, T), dtype=np.uint8)
+        if not dense:
+            expect[0, 4224:4232] = 0
+        assert np.array_equal(g_, expect), bound
+        items = _items_by_start(gr)
+        if dense:
+            r = items[(0, 4224)]
+            assert list(r[:7]) == [4224, -1, 8, 0, 0, 34, 1]
+            masks = [int(x) & 0xFFFFFFFFFFFFFFFF for x in r[7:23]]
+            assert masks[:8] == [usual, usual, usual, odd, usual, usual, usual, usual]
+            assert masks[8:] == [0] * 8 and odd >> 32 == 1 and usual >> 32 == 3
+            # its partner octet 529 stays a uniform single
+            r = items[(0, 4232)]
+            assert r[1] == -1 and r[5] == 16 and r[6] == 0
+            assert list(r[7:23]) == list(range(8)) + list(range(26, 34))
+        else:
+            assert (0, 4224) not in items and (0, 4232) in items
