@@ -79,6 +79,18 @@ def test_forward_matches_oracle(name, dense):
     check_lse(lse, L)
 
 
+def test_forward_dense_bound_64():
+    # one 4500-token document (36 blocks) of random selections: with a bound
+    # of 64 every octet is grouped, and the dense items of blocks 32-35 carry
+    # token masks past bit 31 (the high word of the 64-bit masks)
+    w = _irregular([4500], 31, p_empty=0.1, p_future=0.1)
+    P = oracle.Problem.from_workload(w)
+    O, L = P.forward()
+    o, lse, *_ = run_gpu(w, dense_blocks=64)
+    check_o(o, O)
+    check_lse(lse, L)
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_backward_matches_oracle(name):
     w, O, L, dQ, dK, dV = oracle_results(name)
